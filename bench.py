@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the masked-attention forward hot path on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input:
+attn_build_tiles (slice list -> CSR tile metadata) + attn_fwd, and, for
+workloads that define a KV split, the split partial forwards + attn_merge.
+Default workload: packed varlen causal documents (16384 tokens, 7 documents,
+16 heads, d = 128).  Metric: valid-pair TFLOPS (4 d FLOPs per unmasked
+query-key pair, summed over heads) per second of step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Prints one JSON line.  N > 1 (torchrun) runs N independent replicas, one per
+GPU; the path is not sharded (one GPU per problem), so scaling is "weak".
+"""
+from __future__ import annotations
+
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+METRIC = "masked attn fwd TFLOPS (valid-pair FLOPs) and % of GB300 BF16 dense peak"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="varlen_causal")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK, "fallback"
+
+
+def slices_of(w):
+    from block_sparse_attention_slice_gb300 import attn_slices_from_block_grid
+    if w.grid is not None:
+        return attn_slices_from_block_grid(w.grid, w.block, w.block)
+    return w.slices
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.p = None
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.15)
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.strip().splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0])); mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity for one rank)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def profile_traffic(kernel: str, workload: str, src: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current source of the kernel; else None."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    want = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    got, traffic = None, None
+    for ln in open(p):
+        if ln.startswith("source_sha256_16:"):
+            got = ln.split(":", 1)[1].strip()
+        if ln.startswith("dram_bytes_per_launch:"):
+            traffic = float(ln.split(":", 1)[1].strip())
+    return traffic if got == want else None
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+def run_oracle_timed(w, qf, kf, vf, heads, rows_per_head):
+    import oracle
+    threads = max(1, len(os.sched_getaffinity(0)))
+    if w.grid is not None:
+        mask = lambda r: oracle.mask_rows_grid(w.grid, w.block, r, w.S)
+    else:
+        mask = lambda r: oracle.mask_rows(w.slices, r, w.S)
+    rows = None if rows_per_head is None else {h: rows_per_head[h] for h in heads}
+    rows_list = None if rows is None else [rows.get(h, np.zeros(0, np.int64)) for h in range(w.H)]
+    t0 = time.perf_counter()
+    res = oracle.oracle_attention(qf, kf, vf, w.scale, mask, rows=rows_list, heads=heads,
+                                  threads=min(threads, len(heads)))
+    dt = time.perf_counter() - t0
+    pairs = 0
+    for h, (rr, O, L) in res.items():
+        M = mask(rr)
+        pairs += int(M.sum())
+    return dt, pairs, min(threads, len(heads))
+
+
+def cpu_inputs(w):
+    from block_sparse_attention_slice_gb300 import workloads as W
+    q, k, v = W.draw_qkv(w.S, w.H, w.Hk, w.d, w.seed)
+    f = lambda t: t.float().numpy().astype(np.float64)
+    return f(q), f(k), f(v)
+
+
+def sample_plan(w):
+    """Bounded oracle sample of a workload: (heads, rows per head or None, text)."""
+    threads = max(1, len(os.sched_getaffinity(0)))
+    heads = list(range(min(w.H, threads)))
+    if w.S <= 16384:
+        return heads, None, f"all {w.S} rows of heads 0..{len(heads) - 1} ({len(heads)} of {w.H} heads)"
+    from block_sparse_attention_slice_gb300.workloads import sample_rows
+    n = 256
+    rows = {h: sample_rows(w.S, h, n) for h in heads}
+    return heads, rows, (f"{n} seeded sampled rows (default_rng(100+h)) of heads 0..{len(heads) - 1} "
+                         f"({len(heads)} of {w.H} heads)")
+
+
+def reference_arm(args, ws, rank):
+    if rank != 0:
+        return
+    from block_sparse_attention_slice_gb300 import workloads as W
+    w = W.ALL[args.workload]()
+    qf, kf, vf = cpu_inputs(w)
+    heads, rows, text = sample_plan(w)
+    steps = args.steps if args.steps is not None else 10
+    for _ in range(args.warmup):
+        run_oracle_timed(w, qf, kf, vf, heads, rows)
+    times, pairs, cores = [], 0, 1
+    for _ in range(steps):
+        dt, pairs, cores = run_oracle_timed(w, qf, kf, vf, heads, rows)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    val = 4 * w.d * pairs / (ms / 1e3) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "S": w.S, "H": w.H, "Hk": w.Hk, "d": w.d,
+                       "sample": text},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": text},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def gpu_arm(args, ws, rank, local):
+    import torch
+
+    import block_sparse_attention_slice_gb300 as pkg
+    from block_sparse_attention_slice_gb300 import binding as B
+    from block_sparse_attention_slice_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.load()
+    w = W.ALL[args.workload]()
+    sl = slices_of(w)
+    q, k, v = W.draw_qkv(w.S, w.H, w.Hk, w.d, w.seed)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    pinned = B._pinned_slices(sl)
+    ws_bytes = pkg.attn_tiles_workspace_bytes(sl, w.S, w.S, 256, 128)
+    wsbuf = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((w.S, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.H, w.S), dtype=torch.float32, device=dev)
+    split = []
+    for s2 in w.kv_splits:
+        p2 = B._pinned_slices(s2)
+        b2 = torch.empty(pkg.attn_tiles_workspace_bytes(s2, w.S, w.S, 256, 128), dtype=torch.uint8, device=dev)
+        split.append((s2, p2, b2, torch.empty((w.S, w.H, w.d), dtype=torch.float32, device=dev),
+                      torch.empty((w.H, w.S), dtype=torch.float32, device=dev)))
+    mout = torch.empty_like(out) if split else None
+    mlse = torch.empty_like(lse) if split else None
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    tiles0 = pkg.attn_build_tiles(sl, w.S, w.S, ws=wsbuf, host_slices=pinned)
+    nnz, nref, pairs_per_head, status = tiles0.totals()
+    assert status == 0
+    flops = 4.0 * w.d * pairs_per_head * w.H
+    launches_per_step = 3 + 1 + (len(split) * 4 + 1 if split else 0)
+
+    def step(qx, kx, vx, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        t = pkg.attn_build_tiles(sl, w.S, w.S, ws=wsbuf, host_slices=pinned)
+        if ev is not None:
+            ev[1].record(stream)
+        pkg.attn_fwd(qx, kx, vx, t, w.scale, out=out, lse=lse)
+        if ev is not None:
+            ev[2].record(stream)
+        if split:
+            parts = []
+            for s2, p2, b2, o2, l2 in split:
+                t2 = pkg.attn_build_tiles(s2, w.S, w.S, ws=b2, host_slices=p2)
+                pkg.attn_fwd(qx, kx, vx, t2, w.scale, out=o2, lse=l2)
+                parts.append((o2, l2))
+            if ev is not None:
+                ev[3].record(stream)
+            pkg.attn_merge([p[0] for p in parts], [p[1] for p in parts], out=mout, lse=mlse)
+        if ev is not None:
+            ev[4].record(stream)
+
+    steps = args.steps
+    if steps is None:
+        # a timed region of roughly two seconds, for the clock samples
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(3):
+            step(qd, kd, vd)
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 3
+        steps = int(min(5000, max(10, 2.0 / max(per, 1e-6))))
+    for _ in range(max(3, args.warmup)):
+        step(qd, kd, vd)
+    torch.cuda.synchronize()
+    rc = pkg.attn_last_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    clocks = Clocks(local) if rank == 0 else None
+    barrier(ws)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()                       # L2 flush between timed steps (not timed)
+        step(qd, kd, vd, evs[i])
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop() if clocks else None
+    rc = pkg.attn_last_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} in the timed region")
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    build_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    ms = reduce_max(statistics.mean(step_ms), ws, dev)
+    fwd_mean = statistics.mean(fwd_ms)
+    split_flops = 0.0
+    merge_ms = None
+    if split:
+        split_flops = flops     # the split partials cover exactly the same valid pairs
+        merge_ms = statistics.mean([e[3].elapsed_time(e[4]) for e in evs])
+    step_flops = flops + split_flops
+    value = ws * step_flops / (ms / 1e3) / 1e12
+
+    # ------------------------------------------------ end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        n_e2e = max(3, min(steps, 50))
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for i in range(n_e2e + 2):
+            flush.zero_()
+            es.record(stream)
+            qx = qh.to(dev, non_blocking=True)
+            kx = kh.to(dev, non_blocking=True)
+            vx = vh.to(dev, non_blocking=True)
+            step(qx, kx, vx)
+            res = mout if split else out
+            resl = mlse if split else lse
+            oh.copy_(res, non_blocking=True)
+            lh.copy_(resl, non_blocking=True)
+            ee.record(stream)
+            ee.synchronize()
+            if i >= 2:
+                tot += es.elapsed_time(ee)
+        e2e_ms = reduce_max(tot / n_e2e, ws, dev)
+        h2d = (q.numel() + k.numel() + v.numel()) * 2 + sum(int(x[1]) * 20 for x in [pinned] + [s[1] for s in split])
+        d2h = out.numel() * 2 + lse.numel() * 4
+        e2e = {"value": ws * step_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    pk, pk_src = peaks()
+    fwd_s = fwd_mean / 1e3
+    achieved = flops / fwd_s / 1e12
+    src = os.path.join(ROOT, "block_sparse_attention_slice_gb300", "csrc", "fwd_tcgen05.cu")
+    traffic = profile_traffic("attn_fwd", w.name, src)
+    roof = {"kernel": "attn_fwd", "bound": "tensor", "achieved": achieved,
+            "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+            "traffic": traffic, "peak_source": f"bf16_tflops (burst) of {pk_src}",
+            "fwd_ms": fwd_mean, "build_ms": statistics.mean(build_ms)}
+    extra = {}
+    if split:
+        n = len(split)
+        merge_bytes = w.S * w.H * (n * (4 * w.d + 4) + 2 * w.d + 4)
+        extra["merge"] = {"ms": merge_ms, "achieved_gbs": merge_bytes / (merge_ms / 1e3) / 1e9,
+                          "peak_gbs": pk["hbm_gbs"],
+                          "frac": merge_bytes / (merge_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                          "bytes": merge_bytes}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        qf, kf, vf = (t.float().numpy().astype(np.float64) for t in (q, k, v))
+        heads, rows, text = sample_plan(w)
+        dt, sp, cores = run_oracle_timed(w, qf, kf, vf, heads, rows)
+        cpu = {"value": 4 * w.d * sp / dt / 1e12, "unit": "TFLOP/s", "cores": cores,
+               "kind": "oracle", "sample": text, "seconds": dt}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": steps,
+                "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded numpy normals rounded to bf16)",
+                "config": {"workload": w.name, "S": w.S, "H": w.H, "Hk": w.Hk, "d": w.d,
+                           "valid_pairs_per_head": pairs_per_head, "tiles_nnz": nnz,
+                           "kv_split_parts": len(split), "l2": "flushed between timed steps",
+                           "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+                "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16_tflops"],
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * steps, "clocks": clk, **extra}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        reference_arm(args, ws, rank)
+    else:
+        gpu_arm(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,33 @@
+// Declarations shared by the translation units of the library (host side).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "../../include/attn_slice.h"
+
+namespace attn {
+
+struct BuildLaunch {
+  const attn_slice_t *slices;
+  int n_slices, sq, sk, tq, tk, nq, nk;
+  int32_t *nnz_q, *nref_q, *ref_base_q;
+  int64_t *pairs_q;
+  int32_t *row_ptr, *col_idx, *pairs, *ref_ptr, *ref_idx, *sched;
+  uint8_t *kind;
+  int64_t *totals;
+  int64_t cap_entries, cap_refs;
+};
+
+int build_tiles_launch(const BuildLaunch &b, cudaStream_t s);
+
+int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int hq, int hk, int d,
+               float scale, const attn_tiles_t *tiles, void *out, int out_dtype, float *lse,
+               cudaStream_t stream);
+int fwd_status_take(unsigned int *status);
+void fwd_set_wait_ns(unsigned long long ns);
+int selftest_timeout_launch(cudaStream_t s);
+
+int merge_launch(const void *const *o_parts, const float *const *lse_parts, int n_parts,
+                 int part_dtype, int s_len, int h, int d, void *out, int out_dtype, float *lse,
+                 cudaStream_t s);
+
+}  // namespace attn

@@ -1,0 +1,212 @@
+/*
+ * attn_slice.h -- C ABI of a GB300 (sm_103a) masked-attention forward.
+ *
+ * Three operations, all enqueued on the caller's CUDA stream:
+ *
+ *   attn_build_tiles  slice list -> tile metadata with CSR key-tile lists
+ *   attn_fwd          O = softmax(scale * Q K^T + mask) V and the row LSE
+ *   attn_merge        exact combination of KV-split partial (O, lse) pairs
+ *
+ * Sources (web pages on flexible-mask / block-sparse attention):
+ *   - MagiAttention v1.1.0 release page (xinfinite.net, "Blackwell adaptation"
+ *     bullets): flexible masks as slices, an efficient block-sparse mask
+ *     generation operator that never materialises the full mask, CSR
+ *     compression of the mask metadata, register-to-predicate boundary checks,
+ *     a thin launch path.
+ *   - UltraAttn blog page (blog.ulna520.top), section 3: Full / Causal / Empty
+ *     blocks of the two-dimensional attention matrix, Empty blocks skipped;
+ *     section 3.2: per-KV-shard summaries (m, l, o) merged by the global max.
+ *   - FlashAttention-4 news page (163.com): conditional softmax rescaling and
+ *     the asynchronous MMA + tensor-memory pipeline on Blackwell.
+ *
+ * Conventions
+ *   - No call allocates device memory: the caller owns every buffer.
+ *   - Pointers named d_* / q, k, v, out, lse are device pointers; h_* are host.
+ *   - Every call returns ATTN_OK (0) or an ATTN_ERR_* code.  Argument errors
+ *     are found on the host before anything is launched.  Errors raised inside
+ *     a kernel (a bounded wait that ran out, metadata capacity) are recorded on
+ *     the device and returned by attn_last_device_error().
+ *   - Calls are asynchronous with respect to the host unless stated.
+ *   - Layouts (row-major, elements contiguous in the last index):
+ *       Q   [S_q, H,   d] bf16        K, V [S_k, H_k, d] bf16
+ *       O   [S_q, H,   d] bf16 or f32 lse  [H, S_q] f32 (natural log)
+ *     All of q, k, v, out must be 16-byte aligned; they must not alias out.
+ */
+#ifndef ATTN_SLICE_H
+#define ATTN_SLICE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (0 = the legacy default stream). */
+typedef struct CUstream_st *attn_stream_t;
+
+/* ---- status codes ------------------------------------------------------ */
+#define ATTN_OK              0
+#define ATTN_ERR_INVALID_ARG 1  /* bad size, range, type, null pointer        */
+#define ATTN_ERR_OVERLAP     2  /* two slices' rectangles intersect            */
+#define ATTN_ERR_UNSUPPORTED 3  /* head dim, tile shape, alignment not served  */
+#define ATTN_ERR_CAPACITY    4  /* workspace too small for the metadata        */
+#define ATTN_ERR_CUDA        5  /* a CUDA runtime call failed                  */
+#define ATTN_ERR_TIMEOUT     6  /* a bounded device wait ran out (no hang)     */
+
+/* ---- mask slice kinds ----------------------------------------------------
+ * Local coordinates a = i - q_start, b = j - k_start, L_q = q_end - q_start,
+ * L_k = k_end - k_start.  The pages name these kinds without defining them;
+ * the reading used here is:
+ *   FULL        every (i, j) of the rectangle
+ *   CAUSAL      b <= a + (L_k - L_q)     bottom-right aligned
+ *   INV_CAUSAL  b >= a                   top-left aligned
+ *   BI_CAUSAL   both                                                          */
+#define ATTN_MASK_FULL       0
+#define ATTN_MASK_CAUSAL     1
+#define ATTN_MASK_INV_CAUSAL 2
+#define ATTN_MASK_BI_CAUSAL  3
+
+/* ---- tile kinds (UltraAttn page, section 3: Full / Causal / Empty) ------- */
+#define ATTN_TILE_FULL   1   /* every pair valid: no per-element mask       */
+#define ATTN_TILE_MASKED 2   /* some pairs valid: masked from slice refs    */
+                             /* Empty tiles have no entry at all            */
+/* ---- block-grid kinds (attn_slices_from_block_grid input) --------------- */
+#define ATTN_GRID_EMPTY  0
+#define ATTN_GRID_FULL   1
+#define ATTN_GRID_CAUSAL 2
+
+/* ---- element types ------------------------------------------------------ */
+#define ATTN_DTYPE_BF16 0
+#define ATTN_DTYPE_F32  1
+
+/* Forward kernel tile shape: 256 query rows (two 128-row MMA tiles) by 128
+ * keys.  attn_fwd requires tiles built with exactly this shape. */
+#define ATTN_FWD_TILE_Q 256
+#define ATTN_FWD_TILE_K 128
+#define ATTN_MERGE_MAX_PARTS 16
+
+/* One mask slice, half-open ranges [q_start, q_end) x [k_start, k_end). */
+typedef struct {
+  int32_t q_start, q_end, k_start, k_end, type;
+} attn_slice_t;
+
+/* Tile metadata.  Filled by attn_build_tiles; every pointer points into the
+ * caller's workspace on the device and stays valid while it lives.
+ *   row_ptr [n_qtiles+1]  CSR row pointers over query tiles
+ *   col_idx [nnz]         key-tile index, ascending within a query tile
+ *   kind    [nnz]         ATTN_TILE_FULL or ATTN_TILE_MASKED
+ *   pairs   [nnz]         exact number of valid (query, key) pairs in the tile
+ *   ref_ptr [nnz+1]       entry e uses ref_idx[ref_ptr[e] .. ref_ptr[e+1])
+ *   ref_idx [nref]        ids of the slices with valid pairs in a MASKED tile,
+ *                         ascending; FULL tiles reference none
+ *   sched   [n_qtiles]    query tiles by descending entry count, ties by
+ *                         ascending index (longest-processing-time order)
+ *   totals  [4]           nnz, nref, total valid pairs, device status code
+ *   slices  [n_slices]    device copy of the slice list                   */
+typedef struct {
+  int32_t sq, sk, tile_q, tile_k, n_qtiles, n_ktiles, n_slices, reserved;
+  int64_t cap_entries, cap_refs;
+  int32_t *row_ptr, *col_idx, *pairs, *ref_ptr, *ref_idx, *sched;
+  uint8_t *kind;
+  int64_t *totals;
+  attn_slice_t *slices;
+  int32_t *scratch;      /* per-query-tile counters used while building */
+} attn_tiles_t;
+
+/* Workspace needed by attn_build_tiles for this slice list (host call, no
+ * device work).  The bound counts, per slice, the tiles its rectangle
+ * touches, so it never undercounts.  Errors: INVALID_ARG on a bad size or
+ * slice (same checks as attn_build_tiles, without the overlap test). */
+int attn_tiles_workspace_bytes(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
+                               int tile_q, int tile_k, size_t *bytes);
+
+/* Slice list -> tile metadata (MagiAttention page: block-sparse mask
+ * generation without materialising the mask, CSR-compressed metadata;
+ * UltraAttn page, section 3: Full / Causal / Empty tiles).
+ *   h_slices   host array of n_slices slices (n_slices >= 0; empty slices
+ *              are allowed and ignored); must be pairwise disjoint
+ *   sq, sk     query / key sequence lengths (>= 1)
+ *   tile_q/k   tile shape, 1..1024 each; ceil(sk / tile_k) <= 8192
+ *   d_ws       device workspace of ws_bytes >= attn_tiles_workspace_bytes()
+ *   tiles      host struct, filled with the shape and device pointers
+ * The slice list is copied to the device on `stream`; the metadata is
+ * produced by three kernels on `stream`.  The counts are exact integers, so
+ * the result is bit-identical run to run.  Errors: INVALID_ARG, OVERLAP,
+ * UNSUPPORTED (tile or grid too large), CAPACITY (ws_bytes too small), CUDA. */
+int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
+                     int tile_q, int tile_k, void *d_ws, size_t ws_bytes,
+                     attn_tiles_t *tiles, attn_stream_t stream);
+
+/* Copies totals[0..3] (nnz, nref, total valid pairs, status) to the host;
+ * synchronises `stream` first. */
+int attn_tiles_totals(const attn_tiles_t *tiles, int64_t h_totals[4], attn_stream_t stream);
+
+/* Full / Causal / Empty block grid -> slice list (host only).  One slice per
+ * non-Empty block, in row-major block order: FULL -> a full slice of the
+ * block, CAUSAL -> a causal slice of the block (requires block_q == block_k).
+ *   h_grid     uint8 [nbq * nbk] of ATTN_GRID_*
+ *   h_out      room for `capacity` slices; *n_out receives the count
+ * Errors: INVALID_ARG (bad kind, causal on a non-square block), CAPACITY. */
+int attn_slices_from_block_grid(const uint8_t *h_grid, int nbq, int nbk, int block_q, int block_k,
+                                attn_slice_t *h_out, int capacity, int *n_out);
+
+/* Masked attention forward (UltraAttn page, section 3.3: for a fixed query
+ * tile merge over its valid KV tiles, skip Empty ones; FlashAttention-4 page:
+ * asynchronous MMA with tensor-memory accumulators, conditional rescaling).
+ *   q, k, v     bf16 device tensors in the layouts above
+ *   sq, sk      sequence lengths (must equal tiles->sq, tiles->sk)
+ *   hq, hk      query / key-value heads, hq % hk == 0 (grouped-query heads)
+ *   d           head dim, 64 or 128
+ *   scale       softmax scale (> 0, finite), applied to q . k
+ *   tiles       metadata from attn_build_tiles with tile shape
+ *               ATTN_FWD_TILE_Q x ATTN_FWD_TILE_K
+ *   out         [sq, hq, d] of out_dtype (ATTN_DTYPE_BF16 or _F32)
+ *   lse         [hq, sq] f32: ln sum exp(scale q.k) over valid keys
+ * A query row with no valid key gets O = 0 and lse = -inf.
+ * Errors: INVALID_ARG, UNSUPPORTED (d, tile shape, misaligned pointer), CUDA;
+ * a stalled pipeline stage gives up after a bounded wait and is reported by
+ * attn_last_device_error() as TIMEOUT. */
+int attn_fwd(const void *q, const void *k, const void *v, int sq, int sk, int hq, int hk, int d,
+             float scale, const attn_tiles_t *tiles, void *out, int out_dtype, float *lse,
+             attn_stream_t stream);
+
+/* Exact merge of KV-split partials (UltraAttn page, section 3.2): with
+ * m = max_i lse_i, w_i = exp(lse_i - m), L = sum_i w_i:
+ *   lse = m + ln L,   O = sum_i (w_i / L) O_i.
+ * Partials with lse_i = -inf drop out; if every partial is -inf, O = 0 and
+ * lse = -inf.
+ *   h_o_parts    host array of n_parts device pointers to [s_len, h, d] O_i
+ *                of part_dtype (16-byte aligned)
+ *   h_lse_parts  host array of n_parts device pointers to [h, s_len] f32
+ *   n_parts      1..ATTN_MERGE_MAX_PARTS
+ *   out, lse     [s_len, h, d] of out_dtype, [h, s_len] f32 (may not alias
+ *                the inputs)
+ * Errors: INVALID_ARG, UNSUPPORTED (d not in {64, 128}, alignment), CUDA. */
+int attn_merge(const void *const *h_o_parts, const float *const *h_lse_parts, int n_parts,
+               int part_dtype, int s_len, int h, int d, void *out, int out_dtype, float *lse,
+               attn_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device-side status of
+ * the forward kernels on the current device: ATTN_OK, or ATTN_ERR_TIMEOUT when
+ * a bounded wait ran out (the kernel then left its outputs incomplete). */
+int attn_last_device_error(attn_stream_t stream);
+
+/* Sets the bound on every device-side wait of later attn_fwd launches on the
+ * current process (nanoseconds; default 4e9).  Used to test the timeout path
+ * with a short limit. */
+int attn_set_wait_limit_ns(int64_t ns);
+
+/* Failure-path self test: launches one CTA that waits, with the current wait
+ * bound, on a barrier nothing will ever complete; the wait gives up, records
+ * ATTN_ERR_TIMEOUT in the device status and the kernel returns normally.  Read
+ * the result with attn_last_device_error(). */
+int attn_selftest_wait_timeout(attn_stream_t stream);
+
+/* Human-readable text of a status code (static storage). */
+const char *attn_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ATTN_SLICE_H */

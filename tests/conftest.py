@@ -1,6 +1,11 @@
 import os
 import sys
 
+# The oracle parallelises over heads with threads; one BLAS thread each keeps
+# the thread count equal to the cores used.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))

@@ -1,0 +1,75 @@
+"""The C-ABI library (CPU only): it loads, exports every entry point that
+include/attn_slice.h declares, and its host-only logic (block grid -> slices,
+workspace sizing, argument checks done before any CUDA call) behaves."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from block_sparse_attention_slice_gb300 import binding as B
+from block_sparse_attention_slice_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_attention_slice_gb300 import _build
+    _build.build()
+    return B.load()
+
+
+def _declared():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^(?:const\s+)?[a-z_0-9]+\s*\*?\s*(attn_[a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 10, names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(B.EXPORTS) == names
+
+
+def test_block_grid_to_slices_matches_oracle(lib):
+    w = W.block_sparse_strided()
+    got = B.attn_slices_from_block_grid(w.grid, 128, 128)
+    assert np.array_equal(got, oracle.oracle_slices_from_grid(w.grid, 128))
+    g = np.array([[2, 0], [1, 2]], np.uint8)
+    assert np.array_equal(B.attn_slices_from_block_grid(g, 64, 64),
+                          [[0, 64, 0, 64, 1], [64, 128, 0, 64, 0], [64, 128, 64, 128, 1]])
+    with pytest.raises(B.AttnError):
+        B.attn_slices_from_block_grid(g, 64, 32)          # causal block must be square
+    with pytest.raises(B.AttnError):
+        B.attn_slices_from_block_grid(np.array([[3]], np.uint8), 64, 64)
+
+
+def test_workspace_bound_and_argument_checks(lib):
+    sl = np.array([[0, 512, 0, 512, 1]], np.int32)
+    n = B.attn_tiles_workspace_bytes(sl, 512, 512, 256, 128)
+    assert n > 0 and n % 256 == 0
+    with pytest.raises(B.AttnError) as e:
+        B.attn_tiles_workspace_bytes(np.array([[0, 513, 0, 10, 0]], np.int32), 512, 512, 256, 128)
+    assert e.value.code == B.ATTN_ERR_INVALID_ARG
+    with pytest.raises(B.AttnError) as e:
+        B.attn_tiles_workspace_bytes(np.array([[0, 5, 0, 10, 7]], np.int32), 512, 512, 256, 128)
+    assert e.value.code == B.ATTN_ERR_INVALID_ARG
+    with pytest.raises(B.AttnError) as e:
+        B.attn_tiles_workspace_bytes(sl, 512, 512, 2048, 128)
+    assert e.value.code == B.ATTN_ERR_UNSUPPORTED
+    # overlap is found on the host, before anything touches the device
+    arr, cnt = B._slice_array(np.array([[0, 100, 0, 100, 0], [99, 150, 99, 150, 1]], np.int32))
+    st = B.AttnTiles()
+    rc = lib.attn_build_tiles(arr, cnt, 512, 512, 256, 128, ctypes.c_void_p(256), 1 << 20,
+                              ctypes.byref(st), None)
+    assert rc == B.ATTN_ERR_OVERLAP
+    assert lib.attn_strerror(B.ATTN_ERR_TIMEOUT).decode().startswith("a bounded")

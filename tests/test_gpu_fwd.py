@@ -1,0 +1,168 @@
+"""attn_fwd / attn_merge on the GPU vs the fp64 oracle on identical seeded inputs.
+
+Workloads: the five problem configurations (tiny causal with a 2-way KV
+split, packed varlen causal documents, a block-sparse strided grid, a
+video-generation slice list, a long GQA causal problem with an 8-way KV
+split), plus fuzzed slice lists over all four slice kinds with ragged sizes,
+both head dims, grouped heads, closed-form uniform-score cases and an
+Empty-tile poisoning check.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_attention_slice_gb300 import (attn_build_tiles, attn_fwd, attn_merge,
+                                                attn_slices_from_block_grid)
+from block_sparse_attention_slice_gb300 import workloads as W
+from parity import SAMPLE_ROWS, compare, f64, mask_fn, rows_per_head, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _qkv(w):
+    q, k, v = W.draw_qkv(w.S, w.H, w.Hk, w.d, w.seed)
+    return q, k, v, q.cuda(), k.cuda(), v.cuda()
+
+
+def _slices(w):
+    if w.grid is not None:
+        return attn_slices_from_block_grid(w.grid, w.block, w.block)
+    return w.slices
+
+
+def _split_and_merge(w, qd, kd, vd):
+    parts = []
+    for sl in w.kv_splits:
+        t = attn_build_tiles(sl, w.S, w.S)
+        parts.append(attn_fwd(qd, kd, vd, t, w.scale, out_dtype=torch.float32))
+    return parts, attn_merge([p[0] for p in parts], [p[1] for p in parts])
+
+
+def test_tiny_causal_and_kv_split():
+    w = W.tiny_causal()
+    q, k, v, qd, kd, vd = _qkv(w)
+    ref = run_oracle(q, k, v, w.scale, mask_fn(w))
+    out, lse = attn_fwd(qd, kd, vd, attn_build_tiles(w.slices, w.S, w.S), w.scale)
+    compare(out, lse, ref)
+    parts, (mo, ml) = _split_and_merge(w, qd, kd, vd)
+    compare(mo, ml, ref)
+    # each partial against the oracle of its own slice list
+    for sl, (po, pl) in zip(w.kv_splits, parts):
+        compare(po, pl, run_oracle(q, k, v, w.scale, mask_fn(w, sl)))
+
+
+def test_varlen_causal_all_rows():
+    w = W.varlen_causal()
+    q, k, v, qd, kd, vd = _qkv(w)
+    out, lse = attn_fwd(qd, kd, vd, attn_build_tiles(w.slices, w.S, w.S), w.scale)
+    compare(out, lse, run_oracle(q, k, v, w.scale, mask_fn(w)))
+
+
+def test_block_sparse_strided_sampled():
+    w = W.block_sparse_strided()
+    q, k, v, qd, kd, vd = _qkv(w)
+    out, lse = attn_fwd(qd, kd, vd, attn_build_tiles(_slices(w), w.S, w.S), w.scale)
+    rows = rows_per_head(w, extra=(0, 127, 128, 255, 256, w.S - 1))
+    compare(out, lse, run_oracle(q, k, v, w.scale, mask_fn(w), rows=rows))
+
+
+def test_video_slice_list_sampled():
+    w = W.video_gen()
+    q, k, v, qd, kd, vd = _qkv(w)
+    out, lse = attn_fwd(qd, kd, vd, attn_build_tiles(w.slices, w.S, w.S), w.scale)
+    extra = [0, 4095, 4096, 8191, w.S - 1] + [int(x) for s in w.slices for x in (s[0], s[1] - 1)]
+    rows = rows_per_head(w, extra=extra)
+    compare(out, lse, run_oracle(q, k, v, w.scale, mask_fn(w), rows=rows))
+
+
+@pytest.mark.slow
+def test_long_gqa_causal_whole_and_kv_split_sampled():
+    w = W.gqa_causal_kv_split()
+    q, k, v, qd, kd, vd = _qkv(w)
+    out, lse = attn_fwd(qd, kd, vd, attn_build_tiles(w.slices, w.S, w.S), w.scale)
+    extra = [0, 127, 128, w.S - 1] + [c * (w.S // 8) + o for c in range(8) for o in (-1, 0)]
+    rows = rows_per_head(w, extra=extra)
+    ref = run_oracle(q, k, v, w.scale, mask_fn(w), rows=rows)
+    compare(out, lse, ref)
+    del out, lse
+    parts, (mo, ml) = _split_and_merge(w, qd, kd, vd)
+    del parts
+    compare(mo, ml, ref)
+
+
+@pytest.mark.parametrize("seed,sq,sk,H,Hk,d", [
+    (0, 512, 512, 2, 1, 128), (1, 1000, 1100, 4, 2, 64), (2, 700, 1300, 2, 2, 128),
+    (3, 1300, 600, 3, 1, 64), (4, 2304, 2304, 2, 2, 128), (5, 129, 257, 1, 1, 128)])
+def test_fuzzed_slices_all_kinds(seed, sq, sk, H, Hk, d):
+    rng = np.random.default_rng(seed)
+    sl = W.random_slices(sq, sk, 30, seed=seed + 100, unit=1, max_len=max(16, min(sq, sk) // 2))
+    assert len(sl) > 5
+    q = torch.from_numpy(rng.standard_normal((sq, H, d), dtype=np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy(rng.standard_normal((sk, Hk, d), dtype=np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((sk, Hk, d), dtype=np.float32)).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    tiles = attn_build_tiles(sl, sq, sk)
+    for dt in (torch.bfloat16, torch.float32):
+        out, lse = attn_fwd(q.cuda(), k.cuda(), v.cuda(), tiles, scale, out_dtype=dt)
+        ref = oracle.oracle_attention(f64(q), f64(k), f64(v), scale,
+                                      lambda r: oracle.mask_rows(sl, r, sk))
+        compare(out, lse, ref)
+
+
+@pytest.mark.parametrize("kind", [0, 1, 2, 3])
+def test_uniform_scores_give_means(kind):
+    # q = 0: every score is 0, so P = 1 exactly and O is the mean of V over
+    # the valid keys (closed form), lse = ln(count).
+    S, d = 640, 128
+    rng = np.random.default_rng(kind)
+    q = torch.zeros((S, 1, d), dtype=torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((S, 1, d), dtype=np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy(rng.standard_normal((S, 1, d), dtype=np.float32)).to(torch.bfloat16)
+    sl = np.array([[40, 600, 40, 600, kind]], np.int32)
+    out, lse = attn_fwd(q.cuda(), k.cuda(), v.cuda(), attn_build_tiles(sl, S, S), 0.125,
+                        out_dtype=torch.float32)
+    o, l, vv = out.cpu().numpy()[:, 0], lse.cpu().numpy()[0], f64(v)[:, 0]
+    for i in range(S):
+        if not 40 <= i < 600:
+            assert l[i] == -np.inf and np.all(o[i] == 0)
+            continue
+        a = i - 40
+        keys = {0: range(40, 600), 1: range(40, 41 + a), 2: range(40 + a, 600), 3: [40 + a]}[kind]
+        keys = list(keys)
+        assert abs(l[i] - math.log(len(keys))) < 1e-4
+        assert np.abs(o[i] - vv[keys].mean(axis=0)).max() < 1e-4
+
+
+def test_empty_tiles_never_read():
+    # Key tiles [1024, 1536) are Empty for every query tile: poisoning their
+    # K and V with NaN / huge values must leave the output bit-identical.
+    sq, sk, H, d = 1024, 2048, 2, 128
+    rng = np.random.default_rng(3)
+    sl = np.array([[0, 512, 0, 1024, 1], [512, 1024, 0, 700, 0], [512, 1024, 1536, 2048, 2],
+                   [0, 300, 1600, 1900, 3]], np.int32)
+    q = torch.from_numpy(rng.standard_normal((sq, H, d), dtype=np.float32)).to(torch.bfloat16).cuda()
+    k = torch.from_numpy(rng.standard_normal((sk, H, d), dtype=np.float32)).to(torch.bfloat16).cuda()
+    v = torch.from_numpy(rng.standard_normal((sk, H, d), dtype=np.float32)).to(torch.bfloat16).cuda()
+    tiles = attn_build_tiles(sl, sq, sk)
+    assert not np.isin(tiles.to_host()["col_idx"], [8, 9, 10, 11]).any()
+    o1, l1 = attn_fwd(q, k, v, tiles, 0.09)
+    k2, v2 = k.clone(), v.clone()
+    k2[1024:1536] = float("nan")
+    v2[1024:1536] = 65504.0
+    v2[1024:1100] = float("nan")
+    o2, l2 = attn_fwd(q, k2, v2, tiles, 0.09)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_repeat_runs_bit_identical():
+    w = W.tiny_causal()
+    q, k, v, qd, kd, vd = _qkv(w)
+    t = attn_build_tiles(w.slices, w.S, w.S)
+    a = attn_fwd(qd, kd, vd, t, w.scale)
+    b = attn_fwd(qd, kd, vd, t, w.scale)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1])
