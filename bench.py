@@ -240,14 +240,14 @@ def gpu_arm(args, ws, rank, local):
     q, k, v = W.draw_qkv(w.S, w.H, w.Hk, w.d, w.seed)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    pinned = B._pinned_slices(sl)
+    prep = B.host_slices(sl)
     ws_bytes = pkg.attn_tiles_workspace_bytes(sl, w.S, w.S, 256, 128)
     wsbuf = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty((w.S, w.H, w.d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.H, w.S), dtype=torch.float32, device=dev)
     split = []
     for s2 in w.kv_splits:
-        p2 = B._pinned_slices(s2)
+        p2 = B.host_slices(s2)
         b2 = torch.empty(pkg.attn_tiles_workspace_bytes(s2, w.S, w.S, 256, 128), dtype=torch.uint8, device=dev)
         split.append((s2, p2, b2, torch.empty((w.S, w.H, w.d), dtype=torch.float32, device=dev),
                       torch.empty((w.H, w.S), dtype=torch.float32, device=dev)))
@@ -256,7 +256,7 @@ def gpu_arm(args, ws, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    tiles0 = pkg.attn_build_tiles(sl, w.S, w.S, ws=wsbuf, host_slices=pinned)
+    tiles0 = pkg.attn_build_tiles(sl, w.S, w.S, ws=wsbuf, prepared=prep)
     nnz, nref, pairs_per_head, status = tiles0.totals()
     assert status == 0
     flops = 4.0 * w.d * pairs_per_head * w.H
@@ -265,7 +265,7 @@ def gpu_arm(args, ws, rank, local):
     def step(qx, kx, vx, ev=None):
         if ev is not None:
             ev[0].record(stream)
-        t = pkg.attn_build_tiles(sl, w.S, w.S, ws=wsbuf, host_slices=pinned)
+        t = pkg.attn_build_tiles(sl, w.S, w.S, ws=wsbuf, prepared=prep)
         if ev is not None:
             ev[1].record(stream)
         pkg.attn_fwd(qx, kx, vx, t, w.scale, out=out, lse=lse)
@@ -274,7 +274,7 @@ def gpu_arm(args, ws, rank, local):
         if split:
             parts = []
             for s2, p2, b2, o2, l2 in split:
-                t2 = pkg.attn_build_tiles(s2, w.S, w.S, ws=b2, host_slices=p2)
+                t2 = pkg.attn_build_tiles(s2, w.S, w.S, ws=b2, prepared=p2)
                 pkg.attn_fwd(qx, kx, vx, t2, w.scale, out=o2, lse=l2)
                 parts.append((o2, l2))
             if ev is not None:
@@ -350,7 +350,7 @@ def gpu_arm(args, ws, rank, local):
             if i >= 2:
                 tot += es.elapsed_time(ee)
         e2e_ms = reduce_max(tot / n_e2e, ws, dev)
-        h2d = (q.numel() + k.numel() + v.numel()) * 2 + sum(int(x[1]) * 20 for x in [pinned] + [s[1] for s in split])
+        h2d = (q.numel() + k.numel() + v.numel()) * 2 + sum(int(x[1]) * 20 for x in [prep] + [s[1] for s in split])
         d2h = out.numel() * 2 + lse.numel() * 4
         e2e = {"value": ws * step_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}

@@ -111,15 +111,15 @@ def _slice_array(slices) -> ctypes.Array:
     return arr, len(a)
 
 
-def _pinned_slices(slices):
-    """Slice list in page-locked host memory, so that the upload inside
-    attn_build_tiles is a truly asynchronous copy on the caller's stream."""
-    import torch
+def host_slices(slices):
+    """Slice list as a contiguous int32 [n, 5] host array plus its count.
+
+    Pageable memory on purpose: the upload inside attn_build_tiles stages a
+    pageable source before it returns, so the caller may reuse or free the
+    array right away (a page-locked source would be read later, when the
+    stream reaches the copy)."""
     a = np.ascontiguousarray(np.asarray(slices, dtype=np.int32).reshape(-1, 5))
-    t = torch.empty((max(1, len(a)), 5), dtype=torch.int32, pin_memory=True)
-    if len(a):
-        t[:len(a)] = torch.from_numpy(a)
-    return t, len(a)
+    return (a if len(a) else np.zeros((1, 5), np.int32)), len(a)
 
 
 class Tiles:
@@ -177,27 +177,25 @@ def attn_tiles_workspace_bytes(slices, sq: int, sk: int, tile_q: int, tile_k: in
 
 def attn_build_tiles(slices, sq: int, sk: int, tile_q: int = ATTN_FWD_TILE_Q,
                      tile_k: int = ATTN_FWD_TILE_K, ws=None, stream=None, device=None,
-                     host_slices=None) -> Tiles:
+                     prepared=None) -> Tiles:
     """Slice list (``int32[n, 5]``) -> device tile metadata.
 
-    ``host_slices`` may pass a pinned ``(tensor, n)`` pair from
-    ``_pinned_slices`` to skip re-pinning on repeated builds."""
+    ``prepared`` may pass the ``host_slices(slices)`` pair to skip the
+    conversion on repeated builds; ``ws`` a device workspace to reuse."""
     import torch
-    pinned, n = host_slices if host_slices is not None else _pinned_slices(slices)
+    arr, n = prepared if prepared is not None else host_slices(slices)
     if ws is None:
         nbytes = ctypes.c_size_t(0)
-        _check(load().attn_tiles_workspace_bytes(ctypes.c_void_p(pinned.data_ptr()), n, sq, sk,
-                                                 tile_q, tile_k, ctypes.byref(nbytes)),
+        _check(load().attn_tiles_workspace_bytes(arr.ctypes.data, n, sq, sk, tile_q, tile_k,
+                                                 ctypes.byref(nbytes)),
                "attn_tiles_workspace_bytes")
         ws = torch.empty(int(nbytes.value), dtype=torch.uint8, device=device or "cuda")
     st = AttnTiles()
-    _check(load().attn_build_tiles(ctypes.c_void_p(pinned.data_ptr()), n, sq, sk, tile_q, tile_k,
+    _check(load().attn_build_tiles(arr.ctypes.data, n, sq, sk, tile_q, tile_k,
                                    ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.byref(st),
                                    _stream_ptr(stream)),
            "attn_build_tiles")
-    t = Tiles(st, ws, n)
-    t.host_slices = pinned      # keeps the page-locked source alive for the async upload
-    return t
+    return Tiles(st, ws, n)
 
 
 def attn_slices_from_block_grid(grid, block_q: int, block_k: int) -> np.ndarray:

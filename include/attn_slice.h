@@ -130,7 +130,10 @@ int attn_tiles_workspace_bytes(const attn_slice_t *h_slices, int n_slices, int s
  *   tile_q/k   tile shape, 1..1024 each; ceil(sk / tile_k) <= 8192
  *   d_ws       device workspace of ws_bytes >= attn_tiles_workspace_bytes()
  *   tiles      host struct, filled with the shape and device pointers
- * The slice list is copied to the device on `stream`; the metadata is
+ * The slice list is read on the host during the call and its upload is
+ * enqueued on `stream` (cudaMemcpyAsync): a pageable h_slices is staged
+ * before the call returns and may be reused at once; a page-locked one must
+ * stay unchanged until the stream has executed the copy.  The metadata is
  * produced by three kernels on `stream`.  The counts are exact integers, so
  * the result is bit-identical run to run.  Errors: INVALID_ARG, OVERLAP,
  * UNSUPPORTED (tile or grid too large), CAPACITY (ws_bytes too small), CUDA. */
