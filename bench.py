@@ -69,44 +69,89 @@ def slices_of(w):
 
 
 class Clocks:
-    """nvidia-smi sampler running during the timed region."""
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples SM clock and clock-event reasons during the timed region.
 
-    def __init__(self, index: int):
-        self.p = None
+    Reads NVML through ctypes (read-only queries) from a background thread
+    every ~2 ms, so that even a timed region of a few milliseconds is
+    covered; falls back to an ``nvidia-smi -lms 100`` child process."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        import threading
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.proc, self.thread = None, None
+        self.stop_flag = threading.Event()
         try:
-            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
-                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.p = None
-        time.sleep(0.3)
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            handle = ctypes.c_void_p()
+            import torch
+            uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) != 0:
+                cnt = ctypes.c_uint(0)
+                nv.nvmlDeviceGetCount_v2(ctypes.byref(cnt))
+                if cnt.value != 1 or nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(handle)) != 0:
+                    raise OSError("no NVML handle")
+            mx = ctypes.c_uint(0)
+            nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))
+            self.max_mhz = float(mx.value)
+            fn_reason = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+
+            def loop():
+                clk, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+                while not self.stop_flag.is_set():
+                    if nv.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) == 0:
+                        self.samples.append(float(clk.value))
+                    if fn_reason(handle, ctypes.byref(rs)) == 0:
+                        self.reasons |= int(rs.value)
+                    time.sleep(0.002)
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            self.source = "nvml"
+        except (OSError, AttributeError):
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(cuda_index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap,"
+                     "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                     "clocks_event_reasons.hw_thermal_slowdown",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+                time.sleep(0.3)
+            except OSError:
+                self.source = None
 
     def stop(self):
-        if self.p is None:
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+        elif self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            names = ["sw_power_cap", "hw_slowdown", "sw_thermal_slowdown", "hw_thermal_slowdown"]
+            bits = [0x4, 0x8, 0x20, 0x40]
+            for ln in out.strip().splitlines():
+                f = [x.strip() for x in ln.split(",")]
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except (ValueError, IndexError):
+                    continue
+                for b, v in zip(bits, f[2:6]):
+                    if v.lower().startswith("active"):
+                        self.reasons |= b
+        if not self.samples:
             return None
-        time.sleep(0.15)
-        self.p.terminate()
-        out, _ = self.p.communicate(timeout=10)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in out.strip().splitlines():
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 8:
-                continue
-            try:
-                sm.append(float(f[0])); mx.append(float(f[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.samples), "source": self.source,
+                "reasons": sorted(n for b, n in self.REASONS.items() if self.reasons & b)}
 
 
 def dist_init():

@@ -13,13 +13,18 @@
 //   MASKED  (otherwise)        -> references the slices with pairs in it
 // (UltraAttn page, section 3: Full / Causal / Empty blocks).
 //
-// Three launches on one stream:
+// Two launches on one stream:
 //   count  one CTA per query tile: per-key-tile counts in shared memory ->
 //          entries, references and pairs of the query tile
-//   scan   one CTA: exclusive scans -> row pointers, reference bases, totals
-//   fill   one CTA per query tile: recount, compact the entries in ascending
-//          key-tile order, write the ascending slice references, and place
-//          the query tile at its rank of the longest-processing-time order
+//   fill   one CTA per query tile: its offsets (sums over the preceding
+//          query tiles), recount, compact the entries in ascending key-tile
+//          order, write the ascending slice references, and place the query
+//          tile at its rank of the longest-processing-time order; CTA 0 also
+//          writes the totals
+// Counting is warp-parallel over the rows of a (slice, key tile) pair and
+// visits only the key tiles a slice can touch inside the query tile: for
+// every slice kind the row interval's ends never decrease with the row, so
+// the first row's start and the last row's end bound them.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -40,16 +45,37 @@ __device__ __forceinline__ void row_interval(const attn_slice_t &s, int i, int &
   hi = s.k_start + h;
 }
 
-// Valid pairs of slice s inside rows [r0, r1) x columns [c0, c1).
-__device__ __forceinline__ int pairs_in(const attn_slice_t &s, int r0, int r1, int c0, int c1) {
+// Valid pairs of slice s inside rows [r0, r1) x columns [c0, c1), summed by
+// the 32 lanes of a warp over interleaved rows; every lane gets the total.
+__device__ __forceinline__ int warp_pairs_in(const attn_slice_t &s, int r0, int r1, int c0, int c1,
+                                             int lane) {
   const int a = max(r0, s.q_start), b = min(r1, s.q_end);
   int c = 0;
-  for (int i = a; i < b; ++i) {
+  for (int i = a + lane; i < b; i += 32) {
     int lo, hi;
     row_interval(s, i, lo, hi);
     c += max(0, min(hi, c1) - max(lo, c0));
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
   return c;
+}
+
+// Key tiles [*kt0, *kt1] that slice s can touch within rows [r0, r1); empty
+// when *kt1 < *kt0.
+__device__ __forceinline__ void touched_ktiles(const attn_slice_t &s, int r0, int r1, int tk,
+                                               int *kt0, int *kt1) {
+  const int a = max(r0, s.q_start), b = min(r1, s.q_end);
+  int lo, hi, lo2, hi2;
+  row_interval(s, a, lo, hi);
+  row_interval(s, b - 1, lo2, hi2);
+  if (hi2 <= lo) {
+    *kt0 = 1;
+    *kt1 = 0;
+    return;
+  }
+  *kt0 = lo / tk;
+  *kt1 = (hi2 - 1) / tk;
 }
 
 __device__ __forceinline__ bool hits_rows(const attn_slice_t &s, int r0, int r1) {
@@ -97,10 +123,12 @@ __device__ int gather_hits(const BuildLaunch &b, int from, int r0, int r1, int *
 }
 
 // Per-key-tile valid-pair counts (cnt) and numbers of contributing slices
-// (nref) of query tile qt, accumulated in shared memory.
+// (nref) of query tile qt, accumulated in shared memory; each warp takes one
+// (slice, key tile) pair at a time.
 __device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref, int *list,
                                int *sh) {
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int t = threadIdx.x; t < b.nk; t += BT) {
     cnt[t] = 0;
     nref[t] = 0;
@@ -110,10 +138,11 @@ __device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref
     const int m = gather_hits(b, from, r0, r1, list, sh);
     for (int u = 0; u < m; ++u) {
       const attn_slice_t s = b.slices[list[u]];
-      const int kt0 = s.k_start / b.tk, kt1 = (s.k_end - 1) / b.tk;
-      for (int kt = kt0 + threadIdx.x; kt <= kt1; kt += BT) {
-        const int c = pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk));
-        if (c > 0) {
+      int kt0, kt1;
+      touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
+      for (int kt = kt0 + warp; kt <= kt1; kt += BT / 32) {
+        const int c = warp_pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane);
+        if (c > 0 && lane == 0) {
           atomicAdd(&cnt[kt], c);
           atomicAdd(&nref[kt], 1);
         }
@@ -156,75 +185,62 @@ __global__ void __launch_bounds__(BT) count_kernel(const BuildLaunch b) {
   }
 }
 
-// One CTA of 1024 threads: exclusive scans over the query tiles.
-__global__ void __launch_bounds__(1024) scan_kernel(const BuildLaunch b) {
-  __shared__ long long sh_e[1024], sh_r[1024], sh_p[1024];
-  const int per = (b.nq + 1023) / 1024;
-  const int i0 = threadIdx.x * per, i1 = min(i0 + per, b.nq);
-  long long e = 0, r = 0, pr = 0;
-  for (int i = i0; i < i1; ++i) {
-    e += b.nnz_q[i];
-    r += b.nref_q[i];
-    pr += b.pairs_q[i];
-  }
-  sh_e[threadIdx.x] = e;
-  sh_r[threadIdx.x] = r;
-  sh_p[threadIdx.x] = pr;
-  __syncthreads();
-  // inclusive Hillis-Steele scan over the 1024 partial sums
-  for (int o = 1; o < 1024; o <<= 1) {
-    long long ve = 0, vr = 0, vp = 0;
-    if (threadIdx.x >= o) {
-      ve = sh_e[threadIdx.x - o];
-      vr = sh_r[threadIdx.x - o];
-      vp = sh_p[threadIdx.x - o];
-    }
-    __syncthreads();
-    sh_e[threadIdx.x] += ve;
-    sh_r[threadIdx.x] += vr;
-    sh_p[threadIdx.x] += vp;
-    __syncthreads();
-  }
-  long long be = threadIdx.x ? sh_e[threadIdx.x - 1] : 0;
-  long long br = threadIdx.x ? sh_r[threadIdx.x - 1] : 0;
-  for (int i = i0; i < i1; ++i) {
-    b.row_ptr[i] = static_cast<int32_t>(be);
-    b.ref_base_q[i] = static_cast<int32_t>(br);
-    be += b.nnz_q[i];
-    br += b.nref_q[i];
-  }
-  if (threadIdx.x == 1023) {
-    const long long nnz = sh_e[1023], nref = sh_r[1023];
-    b.row_ptr[b.nq] = static_cast<int32_t>(nnz);
-    b.totals[0] = nnz;
-    b.totals[1] = nref;
-    b.totals[2] = sh_p[1023];
-    const bool over = nnz > b.cap_entries || nref > b.cap_refs;
-    b.totals[3] = over ? ATTN_ERR_CAPACITY : ATTN_OK;
-    if (!over) b.ref_ptr[nnz] = static_cast<int32_t>(nref);
-  }
-}
-
 __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
   extern __shared__ int shm[];
   int *cnt = shm, *nref = shm + b.nk, *rpos = shm + 2 * b.nk, *list = shm + 3 * b.nk,
       *sh = list + BT;
   const int qt = blockIdx.x;
+  const int w = b.nnz_q[qt];
 
-  // longest-processing-time rank of this query tile: tiles with more entries
-  // first, ties broken by the lower index
-  {
-    const int w = b.nnz_q[qt];
-    int rank = 0;
-    for (int j = threadIdx.x; j < b.nq; j += BT) {
-      const int wj = b.nnz_q[j];
-      rank += (wj > w || (wj == w && j < qt)) ? 1 : 0;
+  // offsets of this query tile (sums over the preceding ones), and the
+  // longest-processing-time rank: tiles with more entries first, ties broken
+  // by the lower index
+  long long e_before = 0, r_before = 0, e_all = 0, r_all = 0, p_all = 0;
+  int rank = 0;
+  for (int j = threadIdx.x; j < b.nq; j += BT) {
+    const int wj = b.nnz_q[j], rj = b.nref_q[j];
+    rank += (wj > w || (wj == w && j < qt)) ? 1 : 0;
+    if (j < qt) {
+      e_before += wj;
+      r_before += rj;
     }
-    int tot;
-    block_excl_scan(rank, sh, &tot);
-    if (threadIdx.x == 0) b.sched[tot] = qt;
+    if (qt == 0) {
+      e_all += wj;
+      r_all += rj;
+      p_all += b.pairs_q[j];
+    }
   }
-  if (b.totals[3] != ATTN_OK) return;   // capacity exceeded: leave the lists unwritten
+  __shared__ long long red[6][BT / 32];
+  {
+    long long v[6] = {e_before, r_before, e_all, r_all, p_all, rank};
+#pragma unroll
+    for (int k = 0; k < 6; ++k)
+      for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+    if ((threadIdx.x & 31) == 0)
+#pragma unroll
+      for (int k = 0; k < 6; ++k) red[k][threadIdx.x >> 5] = v[k];
+  }
+  __syncthreads();
+  long long tot[6] = {0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int k = 0; k < 6; ++k)
+    for (int u = 0; u < BT / 32; ++u) tot[k] += red[k][u];
+  const long long row_start = tot[0], ref_start = tot[1];
+  if (threadIdx.x == 0) {
+    b.sched[tot[5]] = qt;
+    b.row_ptr[qt] = static_cast<int32_t>(row_start);
+    if (qt == 0) {
+      const bool over = tot[2] > b.cap_entries || tot[3] > b.cap_refs;
+      b.row_ptr[b.nq] = static_cast<int32_t>(tot[2]);
+      b.totals[0] = tot[2];
+      b.totals[1] = tot[3];
+      b.totals[2] = tot[4];
+      b.totals[3] = over ? ATTN_ERR_CAPACITY : ATTN_OK;
+      if (!over) b.ref_ptr[tot[2]] = static_cast<int32_t>(tot[3]);
+    }
+  }
+  // capacity exceeded: leave this tile's lists unwritten (the status says so)
+  if (row_start + w > b.cap_entries || ref_start + b.nref_q[qt] > b.cap_refs) return;
 
   count_tile_row(b, qt, cnt, nref, list, sh);
   const int full = b.tq * b.tk;
@@ -239,8 +255,8 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
       if (cnt[t] != full) r += nref[t];
     }
   int te, tr;
-  int ebase = block_excl_scan(e, sh, &te) + b.row_ptr[qt];
-  int rbase = block_excl_scan(r, sh, &tr) + b.ref_base_q[qt];
+  int ebase = block_excl_scan(e, sh, &te) + static_cast<int>(row_start);
+  int rbase = block_excl_scan(r, sh, &tr) + static_cast<int>(ref_start);
   for (int t = t0; t < t1; ++t) {
     const int c = cnt[t];
     if (c <= 0) continue;
@@ -257,15 +273,17 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
   // slice references of MASKED tiles, ascending slice id: slices are visited
   // in ascending order and each key tile is written by one thread per slice
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int from = 0; from < b.n_slices; from += BT) {
     const int m = gather_hits(b, from, r0, r1, list, sh);
     for (int u = 0; u < m; ++u) {
       const int sid = list[u];
       const attn_slice_t s = b.slices[sid];
-      const int kt0 = s.k_start / b.tk, kt1 = (s.k_end - 1) / b.tk;
-      for (int kt = kt0 + threadIdx.x; kt <= kt1; kt += BT) {
+      int kt0, kt1;
+      touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
+      for (int kt = kt0 + warp; kt <= kt1; kt += BT / 32) {
         if (cnt[kt] <= 0 || cnt[kt] == full) continue;
-        if (pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk)) > 0)
+        if (warp_pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane) > 0 && lane == 0)
           b.ref_idx[rpos[kt]++] = sid;
       }
       __syncthreads();
@@ -289,7 +307,6 @@ int build_tiles_launch(const BuildLaunch &b, cudaStream_t s) {
   }
   if (b.nq > 0) {
     count_kernel<<<b.nq, BT, sm_count, s>>>(b);
-    scan_kernel<<<1, 1024, 0, s>>>(b);
     fill_kernel<<<b.nq, BT, sm_fill, s>>>(b);
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

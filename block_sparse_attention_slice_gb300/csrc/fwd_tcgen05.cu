@@ -10,12 +10,17 @@
 // (FlashAttention-4 page, "conditional softmax rescaling"); the final
 // O = o / l uses the same reference, so the result is exact either way.
 //
-// CTA = 256 query rows of one head (two 128-row MMA tiles, t = 0, 1) and
-// the KV-tile list of that 256-row query tile.  Warp roles (320 threads):
+// Persistent kernel: one CTA per SM walks the work items (query tile, head)
+// in longest-processing-time order with a static stride.  A work item is 256
+// query rows of one head (two 128-row MMA tiles, t = 0, 1) against the
+// KV-tile list of that 256-row query tile.  Warp roles (352 threads):
 //   warps 0-3  softmax of tile 0 (thread = row = tensor-memory lane)
 //   warps 4-7  softmax of tile 1
-//   warp  8    TMA producer: Q once, then K_j, V_j through an NS-slot ring
+//   warp  8    TMA producer: Q of each item, then K_j, V_j through an NS-slot ring
 //   warp  9    tensor-memory allocator and MMA issuer
+//   warp 10    metadata: resolves each tile entry (key tile, kind, the first
+//              two referenced slices) 32 entries at a time into a shared
+//              ring of records, so the softmax never waits on global memory
 // Tensor memory (512 columns): S_0 [0,128)  S_1 [128,256)  O_0 [256,256+D)
 // O_1 [384,384+D).  P (bf16) overwrites the first 64 columns of S_t and is
 // the A operand of O_t += P_t V_j read straight from tensor memory, so the
@@ -24,7 +29,9 @@
 // so the tensor core works on one tile while the softmax warps of the other
 // tile run (FlashAttention-4 page: softmax overlapped with the MMAs).
 // tcgen05 operations of one thread complete in issue order, so when the
-// softmax of tile t sees S_t(j) its previous PV_t(j-1) has completed too.
+// softmax of tile t sees S_t(j) its previous PV_t(j-1) has completed too,
+// and the next item's first QK may be issued while the softmax warps are
+// still storing the previous item's O (its first PV waits for their P).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -42,7 +49,8 @@ __device__ unsigned int g_fwd_status;
 constexpr int BM = 128;           // rows per MMA tile
 constexpr int BN = 128;           // keys per KV tile
 constexpr float TAU = 8.0f;       // lazy-rescale threshold, log2 units
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 352;
+constexpr int RING = 32;          // metadata records in flight
 
 struct FwdParams {
   const int32_t *row_ptr, *col_idx, *ref_ptr, *ref_idx, *sched;
@@ -50,11 +58,20 @@ struct FwdParams {
   const attn_slice_t *slices;
   void *out;
   float *lse;
-  int sq, sk, hq, hk;
+  int sq, sk, hq, hk, n_items;
   int out_f32;
   float scale_log2;               // scale * log2(e)
   unsigned long long wait_ns;
 };
+
+// One resolved tile entry: key tile, kind, reference range and up to two
+// referenced slices inline (more are read from global memory).
+struct __align__(16) Rec {
+  int kt, kind, r0, r1;
+  attn_slice_t s[2];
+  int pad[2];
+};
+static_assert(sizeof(Rec) == 64, "record size");
 
 template <int D, int NS>
 struct Layout {
@@ -63,18 +80,21 @@ struct Layout {
   static constexpr int TILE = NHALF * HALF;          // 128 x D bf16
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TILE;
-  static constexpr int BAR_OFF = KV_OFF + NS * TILE;
-  // barriers: q_full | full[NS] | empty[NS] | s_full[2] | p_full[2] | o_full[2] | drain
-  static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_S = 1 + 2 * NS,
-                       B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2, NBAR = B_DRAIN + 1;
+  static constexpr int REC_OFF = KV_OFF + NS * TILE;
+  static constexpr int BAR_OFF = REC_OFF + RING * 64;
+  // q_full | q_empty | full[NS] | empty[NS] | s_full[2] | p_full[2] | o_full[2] | drain |
+  // rec_full[RING] | rec_empty[RING]
+  static constexpr int B_Q = 0, B_QE = 1, B_FULL = 2, B_EMPTY = 2 + NS, B_S = 2 + 2 * NS,
+                       B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2, B_RF = B_DRAIN + 1,
+                       B_RE = B_RF + RING, NBAR = B_RE + RING;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;
 };
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int *abort,
-                                         uint64_t deadline) {
-  bool ok = mbar_wait_bounded(bar, parity, abort, deadline);
+                                         uint64_t limit) {
+  bool ok = mbar_wait_bounded(bar, parity, abort, limit);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -114,6 +134,34 @@ __device__ __forceinline__ void slice_interval(const attn_slice_t &s, int i, int
   hi = s.k_start + h;
 }
 
+// ORs the valid columns of slice `s` for row `row` inside key tile [c0, c0+128).
+__device__ __forceinline__ void add_mask(const attn_slice_t &s, int row, int c0, uint32_t (&w)[4]) {
+  int lo, hi;
+  slice_interval(s, row, lo, hi);
+  lo = min(max(lo - c0, 0), BN);
+  hi = min(max(hi - c0, 0), BN);
+  if (hi <= lo) return;
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    const int a = min(max(lo - 32 * c, 0), 32), b = min(max(hi - 32 * c, 0), 32);
+    w[c] |= bits_below(b) & ~bits_below(a);
+  }
+}
+
+struct Item {
+  int qt, h, g, e0, n;
+};
+
+__device__ __forceinline__ Item decode(const FwdParams &p, int item) {
+  Item it;
+  it.qt = __ldg(p.sched + item / p.hq);
+  it.h = item % p.hq;
+  it.g = it.h / (p.hq / p.hk);
+  it.e0 = __ldg(p.row_ptr + it.qt);
+  it.n = __ldg(p.row_ptr + it.qt + 1) - it.e0;
+  return it;
+}
+
 template <int D, int NS>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -126,19 +174,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sb + L::BAR_OFF + 8u * i; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
+  Rec *recs = reinterpret_cast<Rec *>(smem + L::REC_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x;
-  const int qt = p.sched[item / p.hq];
-  const int h = item % p.hq;
-  const int g = h / (p.hq / p.hk);
-  const int e0 = p.row_ptr[qt];
-  const int n = p.row_ptr[qt + 1] - e0;
-  const uint64_t deadline = globaltimer_ns() + p.wait_ns;
+  const uint64_t lim = p.wait_ns;
   const uint32_t q_smem = sb + L::Q_OFF, kv_smem = sb + L::KV_OFF;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_Q), 1);
+    mbar_init(bar(L::B_QE), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(L::B_FULL + s), 1);
       mbar_init(bar(L::B_EMPTY + s), 1);
@@ -149,6 +193,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(L::B_O + t), 1);
     }
     mbar_init(bar(L::B_DRAIN), 1);
+    for (int r = 0; r < RING; ++r) {
+      mbar_init(bar(L::B_RF + r), 1);
+      mbar_init(bar(L::B_RE + r), 8);
+    }
     *abort = 0;
     fence_mbar_init();
   }
@@ -168,36 +216,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::TILE);
-      for (int t = 0; t < 2; ++t)
-        for (int hh = 0; hh < L::NHALF; ++hh)
-          tma_load_2d(q_smem + t * L::TILE + hh * L::HALF, &tm_q, bar(L::B_Q), h * D + hh * 64,
-                      qt * 256 + t * BM);
-      int issued = 0;
-      for (int i = 0; i < 2 * n; ++i) {
-        const int slot = i % NS;
-        const uint32_t use = i / NS;
-        if (use > 0 && !mbar_wait_bounded(bar(L::B_EMPTY + slot), (use - 1) & 1, abort, deadline))
+    if (lane == 0) {
+      uint32_t ld = 0, nonempty = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        const Item it = decode(p, item);
+        if (it.n == 0) continue;
+        if (nonempty > 0 && !mbar_wait_bounded(bar(L::B_QE), (nonempty - 1) & 1, abort, lim)) {
+          ok = false;
           break;
-        const int kt = p.col_idx[e0 + (i >> 1)];
-        const CUtensorMap *tm = (i & 1) ? &tm_v : &tm_k;
-        mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::TILE);
-        for (int hh = 0; hh < L::NHALF; ++hh)
-          tma_load_2d(kv_smem + slot * L::TILE + hh * L::HALF, tm, bar(L::B_FULL + slot),
-                      g * D + hh * 64, kt * BN);
-        issued = i + 1;
+        }
+        mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::TILE);
+        for (int t = 0; t < 2; ++t)
+          for (int hh = 0; hh < L::NHALF; ++hh)
+            tma_load_2d(q_smem + t * L::TILE + hh * L::HALF, &tm_q, bar(L::B_Q), it.h * D + hh * 64,
+                        it.qt * 256 + t * BM);
+        ++nonempty;
+        // key-tile index of the next entry is fetched one entry ahead
+        int kt = 0, kt_next = __ldg(p.col_idx + it.e0);
+        for (int i = 0; i < 2 * it.n; ++i, ++ld) {
+          if (!(i & 1)) {
+            kt = kt_next;
+            if ((i >> 1) + 1 < it.n) kt_next = __ldg(p.col_idx + it.e0 + (i >> 1) + 1);
+          }
+          const int slot = ld % NS;
+          const uint32_t use = ld / NS;
+          if (use > 0 && !mbar_wait_bounded(bar(L::B_EMPTY + slot), (use - 1) & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::TILE);
+          for (int hh = 0; hh < L::NHALF; ++hh)
+            tma_load_2d(kv_smem + slot * L::TILE + hh * L::HALF, (i & 1) ? &tm_v : &tm_k,
+                        bar(L::B_FULL + slot), it.g * D + hh * 64, kt * BN);
+        }
       }
       if (*abort) {
         // let the loads already in flight land before the CTA retires
-        wait_drain(bar(L::B_Q), 0, 20000000ull);
-        for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
+        if (nonempty > 0) wait_drain(bar(L::B_Q), (nonempty - 1) & 1, 20000000ull);
+        const uint32_t from = ld > static_cast<uint32_t>(NS) ? ld - NS : 0;
+        for (uint32_t i = from; i < ld; ++i)
           wait_drain(bar(L::B_FULL + i % NS), (i / NS) & 1, 20000000ull);
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);
       auto issue_qk = [&](int t, int slot) {
@@ -218,160 +282,233 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                  smem_desc_sw128(kv_smem + slot * L::TILE + kk * 16 * 128, L::HALF, 1024), IDESC_PV,
                  (first && kk == 0) ? 0u : 1u);
       };
-      bool ok = mbar_wait_bounded(bar(L::B_Q), 0, abort, deadline);
-      if (ok) ok = mbar_wait_bounded(bar(L::B_FULL + 0), 0, abort, deadline);
-      if (ok) {
+      uint32_t ld = 0, nonempty = 0, step = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        const Item it = decode(p, item);
+        const int n = it.n;
+        if (n == 0) continue;
+        ok = mbar_wait_bounded(bar(L::B_Q), nonempty & 1, abort, lim) &&
+             mbar_wait_bounded(bar(L::B_FULL + ld % NS), (ld / NS) & 1, abort, lim);
+        if (!ok) break;
         tc_fence_after();
-        issue_qk(0, 0);
+        issue_qk(0, ld % NS);
         mma_commit(bar(L::B_S + 0));
-        issue_qk(1, 0);
+        issue_qk(1, ld % NS);
         mma_commit(bar(L::B_S + 1));
-        mma_commit(bar(L::B_EMPTY + 0));
-      }
-      for (int j = 0; ok && j < n; ++j) {
-        const int iv = 2 * j + 1, ik = 2 * j + 2;
-        const int sv = iv % NS, sk = ik % NS;
-        if (!mbar_wait_bounded(bar(L::B_FULL + sv), (iv / NS) & 1, abort, deadline)) break;
-        if (!mbar_wait_bounded(bar(L::B_P + 0), j & 1, abort, deadline)) break;
-        tc_fence_after();
-        issue_pv(0, sv, j == 0);
-        if (j == n - 1) mma_commit(bar(L::B_O + 0));
-        const bool more = j + 1 < n;
-        if (more) {
-          if (!mbar_wait_bounded(bar(L::B_FULL + sk), (ik / NS) & 1, abort, deadline)) break;
+        mma_commit(bar(L::B_EMPTY + ld % NS));
+        if (n == 1) mma_commit(bar(L::B_QE));
+        ++ld;
+        for (int j = 0; j < n; ++j, ++step) {
+          const uint32_t vpos = ld, kpos = ld + 1;
+          const bool more = j + 1 < n;
+          if (!mbar_wait_bounded(bar(L::B_FULL + vpos % NS), (vpos / NS) & 1, abort, lim) ||
+              !mbar_wait_bounded(bar(L::B_P + 0), step & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          issue_qk(0, sk);
-          mma_commit(bar(L::B_S + 0));
+          issue_pv(0, vpos % NS, j == 0);
+          if (!more) mma_commit(bar(L::B_O + 0));
+          if (more) {
+            if (!mbar_wait_bounded(bar(L::B_FULL + kpos % NS), (kpos / NS) & 1, abort, lim)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(0, kpos % NS);
+            mma_commit(bar(L::B_S + 0));
+          }
+          if (!mbar_wait_bounded(bar(L::B_P + 1), step & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(1, vpos % NS, j == 0);
+          mma_commit(bar(L::B_EMPTY + vpos % NS));
+          if (!more) mma_commit(bar(L::B_O + 1));
+          if (more) {
+            issue_qk(1, kpos % NS);
+            mma_commit(bar(L::B_S + 1));
+            mma_commit(bar(L::B_EMPTY + kpos % NS));
+            if (j + 2 == n) mma_commit(bar(L::B_QE));
+          }
+          ld += more ? 2 : 1;
         }
-        if (!mbar_wait_bounded(bar(L::B_P + 1), j & 1, abort, deadline)) break;
-        tc_fence_after();
-        issue_pv(1, sv, j == 0);
-        mma_commit(bar(L::B_EMPTY + sv));
-        if (j == n - 1) mma_commit(bar(L::B_O + 1));
-        if (more) {
-          issue_qk(1, sk);
-          mma_commit(bar(L::B_S + 1));
-          mma_commit(bar(L::B_EMPTY + sk));
-        }
+        ++nonempty;
       }
       // every MMA this thread issued completes before tensor memory is freed
       mma_commit(bar(L::B_DRAIN));
       wait_drain(bar(L::B_DRAIN), 0, 20000000ull);
     }
     __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ metadata
+    uint32_t rpos = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      const Item it = decode(p, item);
+      for (int base = 0; base < it.n; base += 32) {
+        const int j = base + lane;
+        if (j < it.n) {
+          const int e = it.e0 + j;
+          Rec r;
+          r.kt = __ldg(p.col_idx + e);
+          r.kind = __ldg(p.kind + e);
+          r.r0 = __ldg(p.ref_ptr + e);
+          r.r1 = __ldg(p.ref_ptr + e + 1);
+          r.pad[0] = r.pad[1] = 0;
+          r.s[0] = attn_slice_t{0, 0, 0, 0, 0};
+          r.s[1] = attn_slice_t{0, 0, 0, 0, 0};
+          if (r.r1 > r.r0) r.s[0] = p.slices[__ldg(p.ref_idx + r.r0)];
+          if (r.r1 > r.r0 + 1) r.s[1] = p.slices[__ldg(p.ref_idx + r.r0 + 1)];
+          const uint32_t pos = rpos + lane;
+          const int slot = pos % RING;
+          if (pos >= RING &&
+              !mbar_wait_bounded(bar(L::B_RE + slot), (pos / RING - 1) & 1, abort, lim)) {
+            ok = false;
+          } else {
+            recs[slot] = r;
+            mbar_arrive(bar(L::B_RF + slot));
+          }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        rpos += min(32, it.n - base);
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2, wl = warp & 3;
-    const int row = qt * 256 + t * BM + wl * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wl * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + 256 + t * 128;
     const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    uint32_t step = 0, rpos = 0, nonempty = 0;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int e = e0 + j;
-      const int kt = __ldg(p.col_idx + e);
-      const int kd = __ldg(p.kind + e);
-      if (!wait_all(bar(L::B_S + t), j & 1, abort, deadline)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32_wait(tS + c * 32, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(r[k]);
-      }
-      if (kd == 2) {
-        // MASKED tile: union of the referenced slices' row intervals as a
-        // 128-bit mask, then a predicated select per element.
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      const Item it = decode(p, item);
+      const int row = it.qt * 256 + t * BM + wl * 32 + lane;
+      const bool live = row < p.sq;
+      const size_t obase = (static_cast<size_t>(row) * p.hq + it.h) * D;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < it.n; ++j, ++step, ++rpos) {
+        const int slot = rpos % RING;
+        if (!wait_all(bar(L::B_RF + slot), (rpos / RING) & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        const Rec &rc = recs[slot];
+        const int kt = rc.kt, kd = rc.kind, r0 = rc.r0, r1 = rc.r1;
         uint32_t w[BN / 32] = {0u, 0u, 0u, 0u};
-        const int r0 = __ldg(p.ref_ptr + e), r1 = __ldg(p.ref_ptr + e + 1);
-        const int c0 = kt * BN;
-        for (int r = r0; r < r1; ++r) {
-          const attn_slice_t sl = p.slices[__ldg(p.ref_idx + r)];
-          int lo, hi;
-          slice_interval(sl, row, lo, hi);
-          lo = min(max(lo - c0, 0), BN);
-          hi = min(max(hi - c0, 0), BN);
-          if (hi <= lo) continue;
+        if (kd == ATTN_TILE_MASKED) {
+          // MASKED tile: union of the referenced slices' row intervals as a
+          // 128-bit mask, then a predicated select per element.
+          const int c0 = kt * BN;
+          if (r1 > r0) add_mask(rc.s[0], row, c0, w);
+          if (r1 > r0 + 1) add_mask(rc.s[1], row, c0, w);
+          for (int r = r0 + 2; r < r1; ++r) add_mask(p.slices[__ldg(p.ref_idx + r)], row, c0, w);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::B_RE + slot));
+        if (!wait_all(bar(L::B_S + t), step & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[BN];
+        {
+          // all four 32-column loads in flight, one wait
+          uint32_t r[BN];
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) {
-            const int a = min(max(lo - 32 * c, 0), 32), b = min(max(hi - 32 * c, 0), 32);
-            w[c] |= bits_below(b) & ~bits_below(a);
+          for (int c = 0; c < BN / 32; ++c)
+            tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < BN; ++k) {
+            asm volatile("" : "+r"(r[k]));
+            s[k] = __uint_as_float(r[k]);
           }
         }
+        if (kd == ATTN_TILE_MASKED) {
 #pragma unroll
-        for (int k = 0; k < BN; ++k)
-          if (!((w[k >> 5] >> (k & 31)) & 1u)) s[k] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int k = 1; k < BN; ++k) mx = fmaxf(mx, s[k]);
-      const float mx2 = mx * sl2;
-      const float m_old = m_ref;
-      const bool grow = mx2 > m_ref + TAU;
-      if (grow) m_ref = mx2;
-      const float factor = grow ? ex2_approx(m_old - m_ref) : 1.f;
-      l *= factor;
-      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * k], sl2, -mb));
-          const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * k + 1], sl2, -mb));
-          l += p0 + p1;
-          pk[k] = pack_bf16x2(p0, p1);
+          for (int k = 0; k < BN; ++k)
+            if (!((w[k >> 5] >> (k & 31)) & 1u)) s[k] = -INFINITY;
         }
-        tmem_st16(tS + c * 16, pk);
-      }
-      const bool rescale = grow && (m_old != -INFINITY) && j > 0;
-      if (__any_sync(0xffffffffu, rescale)) {
+        // row max as a tree: eight independent partial maxima
+        float m8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m8[u] = s[u];
+#pragma unroll
+        for (int k = 8; k < BN; ++k) m8[k & 7] = fmaxf(m8[k & 7], s[k]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        const float mx2 = mx * sl2;
+        const float m_old = m_ref;
+        const bool grow = mx2 > m_ref + TAU;
+        if (grow) m_ref = mx2;
+        const float factor = grow ? ex2_approx(m_old - m_ref) : 1.f;
+        l *= factor;
+        const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};     // four independent partial sums
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * k], sl2, -mb));
+            const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * k + 1], sl2, -mb));
+            l4[k & 3] += p0 + p1;
+            pk[k] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + c * 16, pk);
+        }
+        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        const bool rescale = grow && (m_old != -INFINITY) && j > 0;
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32_wait(tO + c * 32, r);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32_wait(tO + c * 32, r);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * factor);
-          tmem_st32(tO + c * 32, r);
+            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * factor);
+            tmem_st32(tO + c * 32, r);
+          }
         }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::B_P + t));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(L::B_P + t));
-    }
-    // ------------------------------------------------------------ epilogue
-    if (n > 0 && ok) ok = wait_all(bar(L::B_O + t), 0, abort, deadline);
-    if (ok) {
-      tc_fence_after();
-      const bool live = row < p.sq;
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (it.n > 0) {
+        if (!wait_all(bar(L::B_O + t), nonempty & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        ++nonempty;
+        tc_fence_after();
+      }
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        if (n > 0) {
+        if (it.n > 0) {
           tmem_ld32_wait(tO + c * 32, r);
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) r[k] = 0u;
         }
         if (!live) continue;
-        const size_t base = (static_cast<size_t>(row) * p.hq + h) * D + c * 32;
         if (p.out_f32) {
-          float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + base);
+          float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + obase + c * 32);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
                                  __uint_as_float(r[4 * k + 2]) * inv,
                                  __uint_as_float(r[4 * k + 3]) * inv);
         } else {
-          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + base);
+          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + obase + c * 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             uint4 v;
@@ -384,8 +521,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       if (live)
-        p.lse[static_cast<size_t>(h) * p.sq + row] =
+        p.lse[static_cast<size_t>(it.h) * p.sq + row] =
             l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      // tensor-memory reads of O finish before the next item's first PV
+      tc_fence_before();
     }
   }
 
@@ -428,17 +567,33 @@ static int make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t ro
 }
 
 static unsigned long long g_wait_ns = 4000000000ull;
+constexpr int kMaxDev = 64;
+
+static int sm_count() {
+  static int cached[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return -1;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return -1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
 
 template <int D, int NS>
 static int launch_fwd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                       const FwdParams &p, int grid, cudaStream_t s) {
   using L = Layout<D, NS>;
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
+  if (!configured[dev]) {
     if (cudaFuncSetAttribute(fwd_kernel<D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::ALLOC) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    configured = true;
+    configured[dev] = true;
   }
   fwd_kernel<D, NS><<<grid, NTHREADS, L::ALLOC, s>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -469,8 +624,13 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   p.out_f32 = out_dtype == ATTN_DTYPE_F32;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_ns = g_wait_ns;
-  const int grid = tiles->n_qtiles * hq;
-  if (grid == 0) return ATTN_OK;
+  const long long items = static_cast<long long>(tiles->n_qtiles) * hq;
+  if (items == 0) return ATTN_OK;
+  if (items >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  p.n_items = static_cast<int>(items);
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const int grid = static_cast<int>(items < sms ? items : sms);
   if (d == 128) return launch_fwd<128, 4>(mq, mk, mv, p, grid, stream);
   return launch_fwd<64, 8>(mq, mk, mv, p, grid, stream);
 }
@@ -495,8 +655,7 @@ __global__ void selftest_timeout_kernel(unsigned long long wait_ns) {
   mbar_init(a, 1);
   abort_flag = 0;
   fence_mbar_init();
-  const uint64_t dl = globaltimer_ns() + wait_ns;
-  if (!mbar_wait_bounded(a, 0, reinterpret_cast<volatile int *>(&abort_flag), dl))
+  if (!mbar_wait_bounded(a, 0, reinterpret_cast<volatile int *>(&abort_flag), wait_ns))
     atomicExch(&g_fwd_status, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
 }
 

@@ -48,16 +48,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of parity `parity` of barrier `bar` to complete.
-// Gives up (returns false) when *abort becomes non-zero or when the global
-// timer passes `deadline`; in the latter case it raises *abort itself so
-// that every other waiter of the CTA gives up too.
+// Gives up (returns false) when *abort becomes non-zero or when this wait
+// has lasted more than `limit_ns` by the global timer; in the latter case it
+// raises *abort itself so that every other waiter of the CTA gives up too.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int *abort, uint64_t deadline) {
+                                                  volatile int *abort, uint64_t limit_ns) {
+  uint64_t deadline = 0;
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 31u) {
       if (*abort) return false;
-      if (globaltimer_ns() > deadline) {
+      const uint64_t now = globaltimer_ns();
+      if (deadline == 0) {
+        deadline = now + limit_ns;
+      } else if (now > deadline) {
         *abort = 1;
         return false;
       }
