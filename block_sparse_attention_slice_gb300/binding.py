@@ -23,7 +23,8 @@ ATTN_FWD_TILE_Q, ATTN_FWD_TILE_K = 256, 128
 ATTN_MERGE_MAX_PARTS = 16
 
 # every entry point declared in include/attn_slice.h
-EXPORTS = ["attn_tiles_workspace_bytes", "attn_build_tiles", "attn_tiles_totals",
+EXPORTS = ["attn_tiles_workspace_bytes", "attn_build_tiles", "attn_build_tiles_noalloc",
+           "attn_tiles_totals",
            "attn_slices_from_block_grid", "attn_fwd", "attn_merge", "attn_last_device_error",
            "attn_set_wait_limit_ns", "attn_selftest_wait_timeout", "attn_strerror"]
 
@@ -67,6 +68,8 @@ def load(path: Optional[str] = None):
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     lib.attn_tiles_workspace_bytes.argtypes = [vp, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
     lib.attn_build_tiles.argtypes = [vp, i32, i32, i32, i32, i32, vp, sz, ctypes.POINTER(AttnTiles), vp]
+    lib.attn_build_tiles_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, vp, sz,
+                                             ctypes.POINTER(AttnTiles), vp]
     lib.attn_tiles_totals.argtypes = [ctypes.POINTER(AttnTiles), ctypes.POINTER(ctypes.c_int64), vp]
     lib.attn_slices_from_block_grid.argtypes = [vp, i32, i32, i32, i32, vp, i32, ctypes.POINTER(ctypes.c_int)]
     lib.attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
@@ -196,6 +199,21 @@ def attn_build_tiles(slices, sq: int, sk: int, tile_q: int = ATTN_FWD_TILE_Q,
                                    _stream_ptr(stream)),
            "attn_build_tiles")
     return Tiles(st, ws, n)
+
+
+def attn_build_tiles_noalloc(slices, sq: int, sk: int, out, tile_q: int = ATTN_FWD_TILE_Q,
+                             tile_k: int = ATTN_FWD_TILE_K, stream=None) -> Tiles:
+    """Like ``attn_build_tiles``, but the library's fixed device array holds
+    the build's scratch counters: nothing is allocated, ``out`` (a uint8 CUDA
+    tensor of at least ``attn_tiles_workspace_bytes`` bytes) receives the
+    metadata.  Calls that overlap on the GPU share that array and race."""
+    arr, n = host_slices(slices)
+    st = AttnTiles()
+    _check(load().attn_build_tiles_noalloc(arr.ctypes.data, n, sq, sk, tile_q, tile_k,
+                                           ctypes.c_void_p(out.data_ptr()), out.numel(),
+                                           ctypes.byref(st), _stream_ptr(stream)),
+           "attn_build_tiles_noalloc")
+    return Tiles(st, out, n)
 
 
 def attn_slices_from_block_grid(grid, block_q: int, block_k: int) -> np.ndarray:

@@ -10,7 +10,8 @@
 
 #include "attn_internal.h"
 
-namespace {
+namespace attn {
+namespace host {
 
 constexpr size_t kAlign = 256;
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -44,12 +45,6 @@ int check_overlap(const attn_slice_t *s, int n) {
   }
   return ATTN_OK;
 }
-
-struct WsLayout {
-  size_t slices, row_ptr, sched, nnz_q, nref_q, ref_base_q, pairs_q, totals, col_idx, pairs,
-      ref_ptr, kind, ref_idx, total;
-  int64_t cap_e, cap_r;
-};
 
 int shape_ok(int sq, int sk, int tq, int tk, int *nq, int *nk) {
   if (sq < 1 || sk < 1 || tq < 1 || tk < 1) return ATTN_ERR_INVALID_ARG;
@@ -97,7 +92,10 @@ WsLayout layout(const attn_slice_t *s, int n, int nq, int nk, int tq, int tk) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-}  // namespace
+}  // namespace host
+}  // namespace attn
+
+using namespace attn::host;
 
 extern "C" {
 

@@ -6,6 +6,19 @@
 
 namespace attn {
 
+// Host-side checks and workspace layout of the tile metadata (attn_api.cu).
+namespace host {
+struct WsLayout {
+  size_t slices, row_ptr, sched, nnz_q, nref_q, ref_base_q, pairs_q, totals, col_idx, pairs,
+      ref_ptr, kind, ref_idx, total;
+  int64_t cap_e, cap_r;
+};
+int check_slices(const attn_slice_t *s, int n, int sq, int sk);
+int check_overlap(const attn_slice_t *s, int n);
+int shape_ok(int sq, int sk, int tq, int tk, int *nq, int *nk);
+WsLayout layout(const attn_slice_t *s, int n, int nq, int nk, int tq, int tk);
+}  // namespace host
+
 struct BuildLaunch {
   const attn_slice_t *slices;
   int n_slices, sq, sk, tq, tk, nq, nk;

@@ -141,6 +141,32 @@ int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
                      int tile_q, int tile_k, void *d_ws, size_t ws_bytes,
                      attn_tiles_t *tiles, attn_stream_t stream);
 
+/* attn_build_tiles without any device memory from the caller beyond the
+ * input slice list and the output buffer.  The pages have no counterpart: it
+ * exists for callers that cannot allocate, or lend, scratch memory at the
+ * moment they build a mask -- for example a serving process whose device
+ * memory is handed out by its own pool fixed at start-up, or a plugin inside
+ * another framework that only receives pre-sized input and output buffers.
+ * The per-query-tile counters that attn_build_tiles keeps in the caller's
+ * workspace live instead in one fixed array inside this library
+ * (ATTN_NOALLOC_MAX_QTILES entries, 20 bytes each, 320 KiB), which every GPU
+ * that loads the library holds until the process exits.
+ *   arguments   as attn_build_tiles; d_out (256-byte aligned) receives the
+ *               metadata and needs out_bytes >= attn_tiles_workspace_bytes()
+ *   limits      ceil(sq / tile_q) <= ATTN_NOALLOC_MAX_QTILES, else CAPACITY
+ * No cudaMalloc, cudaFree or other allocating call is made.  The first call
+ * on a device looks up the array's device address once (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.
+ * All calls share the one array, which keeps the last call's contents (the
+ * kernels overwrite every counter they read, so nothing needs clearing):
+ * calls whose work overlaps on the GPU -- on different streams, or from
+ * different threads -- race on it and must be serialised by the caller.
+ * Errors: as attn_build_tiles. */
+#define ATTN_NOALLOC_MAX_QTILES 16384
+int attn_build_tiles_noalloc(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
+                             int tile_q, int tile_k, void *d_out, size_t out_bytes,
+                             attn_tiles_t *tiles, attn_stream_t stream);
+
 /* Copies totals[0..3] (nnz, nref, total valid pairs, status) to the host;
  * synchronises `stream` first. */
 int attn_tiles_totals(const attn_tiles_t *tiles, int64_t h_totals[4], attn_stream_t stream);
