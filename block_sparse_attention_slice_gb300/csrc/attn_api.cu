@@ -58,22 +58,28 @@ int shape_ok(int sq, int sk, int tq, int tk, int *nq, int *nk) {
 
 WsLayout layout(const attn_slice_t *s, int n, int nq, int nk, int tq, int tk) {
   WsLayout L{};
-  int64_t touched = 0;
+  int64_t touched = 0, touched_q = 0;
   for (int i = 0; i < n; ++i) {
     if (s[i].q_end <= s[i].q_start || s[i].k_end <= s[i].k_start) continue;
     const int64_t a = (s[i].q_end - 1) / tq - s[i].q_start / tq + 1;
     const int64_t b = (s[i].k_end - 1) / tk - s[i].k_start / tk + 1;
     touched += a * b;
+    touched_q += a;
   }
   L.cap_e = std::min<int64_t>(touched, static_cast<int64_t>(nq) * nk);
   L.cap_r = touched;
-  size_t o = 0;
+  L.n_qb = touched_q;
+  // input region: packed back to back (one upload), 4-byte aligned parts
+  L.slices = 0;
+  L.qb_ptr = sizeof(attn_slice_t) * n;
+  L.qb_idx = L.qb_ptr + sizeof(int32_t) * (nq + 1);
+  L.input_bytes = L.qb_idx + sizeof(int32_t) * touched_q;
+  size_t o = up(L.input_bytes);
   auto put = [&](size_t bytes) {
     const size_t at = o;
     o = up(o + std::max<size_t>(bytes, 1));
     return at;
   };
-  L.slices = put(sizeof(attn_slice_t) * n);
   L.row_ptr = put(sizeof(int32_t) * (nq + 1));
   L.sched = put(sizeof(int32_t) * nq);
   L.nnz_q = put(sizeof(int32_t) * nq);
@@ -88,6 +94,24 @@ WsLayout layout(const attn_slice_t *s, int n, int nq, int nk, int tq, int tk) {
   L.ref_idx = put(sizeof(int32_t) * L.cap_r);
   L.total = o;
   return L;
+}
+
+void stage_inputs(const attn_slice_t *s, int n, int nq, int tq, const WsLayout &L,
+                  std::vector<uint8_t> *img) {
+  img->assign(L.input_bytes, 0);
+  if (n > 0) std::memcpy(img->data() + L.slices, s, sizeof(attn_slice_t) * n);
+  int32_t *ptr = reinterpret_cast<int32_t *>(img->data() + L.qb_ptr);
+  int32_t *idx = reinterpret_cast<int32_t *>(img->data() + L.qb_idx);
+  for (int i = 0; i < n; ++i) {
+    if (s[i].q_end <= s[i].q_start || s[i].k_end <= s[i].k_start) continue;
+    for (int q = s[i].q_start / tq; q <= (s[i].q_end - 1) / tq; ++q) ++ptr[q + 1];
+  }
+  for (int q = 0; q < nq; ++q) ptr[q + 1] += ptr[q];
+  std::vector<int32_t> fill(ptr, ptr + nq);
+  for (int i = 0; i < n; ++i) {          // ascending ids within every bucket
+    if (s[i].q_end <= s[i].q_start || s[i].k_end <= s[i].k_start) continue;
+    for (int q = s[i].q_start / tq; q <= (s[i].q_end - 1) / tq; ++q) idx[fill[q]++] = i;
+  }
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -146,11 +170,14 @@ int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
   t.slices = reinterpret_cast<attn_slice_t *>(ws + L.slices);
   t.scratch = reinterpret_cast<int32_t *>(ws + L.nnz_q);
 
-  if (n_slices > 0 && cudaMemcpyAsync(t.slices, h_slices, sizeof(attn_slice_t) * n_slices,
-                                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+  std::vector<uint8_t> img;
+  stage_inputs(h_slices, n_slices, nq, tile_q, L, &img);
+  if (cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
     return ATTN_ERR_CUDA;
   attn::BuildLaunch b;
   b.slices = t.slices;
+  b.qb_ptr = reinterpret_cast<const int32_t *>(ws + L.qb_ptr);
+  b.qb_idx = reinterpret_cast<const int32_t *>(ws + L.qb_idx);
   b.n_slices = n_slices;
   b.sq = sq;
   b.sk = sk;

@@ -2,6 +2,9 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <cstdint>
+#include <vector>
+
 #include "../../include/attn_slice.h"
 
 namespace attn {
@@ -9,18 +12,25 @@ namespace attn {
 // Host-side checks and workspace layout of the tile metadata (attn_api.cu).
 namespace host {
 struct WsLayout {
-  size_t slices, row_ptr, sched, nnz_q, nref_q, ref_base_q, pairs_q, totals, col_idx, pairs,
-      ref_ptr, kind, ref_idx, total;
-  int64_t cap_e, cap_r;
+  // input region (one upload): slices | qb_ptr | qb_idx, then the outputs
+  size_t slices, qb_ptr, qb_idx, input_bytes;
+  size_t row_ptr, sched, nnz_q, nref_q, ref_base_q, pairs_q, totals, col_idx, pairs, ref_ptr,
+      kind, ref_idx, total;
+  int64_t cap_e, cap_r, n_qb;
 };
 int check_slices(const attn_slice_t *s, int n, int sq, int sk);
 int check_overlap(const attn_slice_t *s, int n);
 int shape_ok(int sq, int sk, int tq, int tk, int *nq, int *nk);
 WsLayout layout(const attn_slice_t *s, int n, int nq, int nk, int tq, int tk);
+// Host image of the input region: the slices, then per query tile the ids of
+// the non-empty slices whose rows meet it (CSR, ascending ids).
+void stage_inputs(const attn_slice_t *s, int n, int nq, int tq, const WsLayout &L,
+                  std::vector<uint8_t> *img);
 }  // namespace host
 
 struct BuildLaunch {
   const attn_slice_t *slices;
+  const int32_t *qb_ptr, *qb_idx;   // slices meeting each query tile, ascending ids
   int n_slices, sq, sk, tq, tk, nq, nk;
   int32_t *nnz_q, *nref_q, *ref_base_q;
   int64_t *pairs_q;

@@ -15,7 +15,9 @@
 //
 // Two launches on one stream:
 //   count  one CTA per query tile: per-key-tile counts in shared memory ->
-//          entries, references and pairs of the query tile
+//          entries, references and pairs of the query tile; the slices
+//          visited are the query tile's bucket (built on the host with the
+//          argument checks: ids of the slices meeting its rows, ascending)
 //   fill   one CTA per query tile: its offsets (sums over the preceding
 //          query tiles), recount, compact the entries in ascending key-tile
 //          order, write the ascending slice references, and place the query
@@ -78,10 +80,6 @@ __device__ __forceinline__ void touched_ktiles(const attn_slice_t &s, int r0, in
   *kt1 = (hi2 - 1) / tk;
 }
 
-__device__ __forceinline__ bool hits_rows(const attn_slice_t &s, int r0, int r1) {
-  return s.q_end > s.q_start && s.k_end > s.k_start && s.q_start < r1 && r0 < s.q_end;
-}
-
 // Block-wide exclusive scan of one int per thread (BT threads); returns the
 // prefix and writes the block total to *total.
 __device__ int block_excl_scan(int v, int *sh, int *total) {
@@ -110,23 +108,11 @@ __device__ int block_excl_scan(int v, int *sh, int *total) {
   return before;
 }
 
-// Collects, in ascending order, the ids of the slices that touch rows
-// [r0, r1) into `list` (at most BT per call, starting from slice `from`).
-__device__ int gather_hits(const BuildLaunch &b, int from, int r0, int r1, int *list, int *sh) {
-  const int s = from + threadIdx.x;
-  const int hit = (s < b.n_slices && hits_rows(b.slices[s], r0, r1)) ? 1 : 0;
-  int total;
-  const int pos = block_excl_scan(hit, sh, &total);
-  if (hit) list[pos] = s;
-  __syncthreads();
-  return total;
-}
-
 // Per-key-tile valid-pair counts (cnt) and numbers of contributing slices
-// (nref) of query tile qt, accumulated in shared memory; each warp takes one
-// (slice, key tile) pair at a time.
-__device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref, int *list,
-                               int *sh) {
+// (nref) of query tile qt, accumulated in shared memory; the slices are those
+// of the query tile's bucket, and each warp takes one (slice, key tile) pair
+// at a time.
+__device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref) {
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int t = threadIdx.x; t < b.nk; t += BT) {
@@ -134,29 +120,27 @@ __device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref
     nref[t] = 0;
   }
   __syncthreads();
-  for (int from = 0; from < b.n_slices; from += BT) {
-    const int m = gather_hits(b, from, r0, r1, list, sh);
-    for (int u = 0; u < m; ++u) {
-      const attn_slice_t s = b.slices[list[u]];
-      int kt0, kt1;
-      touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
-      for (int kt = kt0 + warp; kt <= kt1; kt += BT / 32) {
-        const int c = warp_pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane);
-        if (c > 0 && lane == 0) {
-          atomicAdd(&cnt[kt], c);
-          atomicAdd(&nref[kt], 1);
-        }
+  const int u0 = b.qb_ptr[qt], u1 = b.qb_ptr[qt + 1];
+  for (int u = u0; u < u1; ++u) {
+    const attn_slice_t s = b.slices[b.qb_idx[u]];
+    int kt0, kt1;
+    touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
+    for (int kt = kt0 + warp; kt <= kt1; kt += BT / 32) {
+      const int c = warp_pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane);
+      if (c > 0 && lane == 0) {
+        atomicAdd(&cnt[kt], c);
+        atomicAdd(&nref[kt], 1);
       }
     }
-    __syncthreads();
   }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(BT) count_kernel(const BuildLaunch b) {
   extern __shared__ int shm[];
-  int *cnt = shm, *nref = shm + b.nk, *list = shm + 2 * b.nk, *sh = list + BT;
+  int *cnt = shm, *nref = shm + b.nk, *sh = shm + 2 * b.nk;
   const int qt = blockIdx.x;
-  count_tile_row(b, qt, cnt, nref, list, sh);
+  count_tile_row(b, qt, cnt, nref);
   const int full = b.tq * b.tk;
   int e = 0, r = 0;
   long long pr = 0;
@@ -187,8 +171,7 @@ __global__ void __launch_bounds__(BT) count_kernel(const BuildLaunch b) {
 
 __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
   extern __shared__ int shm[];
-  int *cnt = shm, *nref = shm + b.nk, *rpos = shm + 2 * b.nk, *list = shm + 3 * b.nk,
-      *sh = list + BT;
+  int *cnt = shm, *nref = shm + b.nk, *rpos = shm + 2 * b.nk, *sh = shm + 3 * b.nk;
   const int qt = blockIdx.x;
   const int w = b.nnz_q[qt];
 
@@ -242,7 +225,7 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
   // capacity exceeded: leave this tile's lists unwritten (the status says so)
   if (row_start + w > b.cap_entries || ref_start + b.nref_q[qt] > b.cap_refs) return;
 
-  count_tile_row(b, qt, cnt, nref, list, sh);
+  count_tile_row(b, qt, cnt, nref);
   const int full = b.tq * b.tk;
   // entries of this query tile in ascending key-tile order: each thread owns
   // a contiguous run of key tiles so a single scan orders them
@@ -274,26 +257,24 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
   // in ascending order and each key tile is written by one thread per slice
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int from = 0; from < b.n_slices; from += BT) {
-    const int m = gather_hits(b, from, r0, r1, list, sh);
-    for (int u = 0; u < m; ++u) {
-      const int sid = list[u];
-      const attn_slice_t s = b.slices[sid];
-      int kt0, kt1;
-      touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
-      for (int kt = kt0 + warp; kt <= kt1; kt += BT / 32) {
-        if (cnt[kt] <= 0 || cnt[kt] == full) continue;
-        if (warp_pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane) > 0 && lane == 0)
-          b.ref_idx[rpos[kt]++] = sid;
-      }
-      __syncthreads();
+  const int u0 = b.qb_ptr[qt], u1 = b.qb_ptr[qt + 1];
+  for (int u = u0; u < u1; ++u) {
+    const int sid = b.qb_idx[u];
+    const attn_slice_t s = b.slices[sid];
+    int kt0, kt1;
+    touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
+    for (int kt = kt0 + warp; kt <= kt1; kt += BT / 32) {
+      if (cnt[kt] <= 0 || cnt[kt] == full) continue;
+      if (warp_pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane) > 0 && lane == 0)
+        b.ref_idx[rpos[kt]++] = sid;
     }
+    __syncthreads();
   }
 }
 
 int build_tiles_launch(const BuildLaunch &b, cudaStream_t s) {
-  const size_t sm_count = (2 * static_cast<size_t>(b.nk) + BT + 64) * sizeof(int);
-  const size_t sm_fill = (3 * static_cast<size_t>(b.nk) + BT + 64) * sizeof(int);
+  const size_t sm_count = (2 * static_cast<size_t>(b.nk) + 64) * sizeof(int);
+  const size_t sm_fill = (3 * static_cast<size_t>(b.nk) + 64) * sizeof(int);
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);

@@ -90,14 +90,17 @@ extern "C" int attn_build_tiles_noalloc(const attn_slice_t *h_slices, int n_slic
   t.slices = reinterpret_cast<attn_slice_t *>(ws + L.slices);
   t.scratch = reinterpret_cast<int32_t *>(sc);
 
-  if (n_slices > 0 && cudaMemcpyAsync(t.slices, h_slices, sizeof(attn_slice_t) * n_slices,
-                                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+  std::vector<uint8_t> img;
+  stage_inputs(h_slices, n_slices, nq, tile_q, L, &img);
+  if (cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  // The counters are written (not accumulated) by the count and scan
-  // kernels before anything reads them, so the previous call's contents in
+  // The counters are written (not accumulated) by the count kernel before
+  // the fill kernel reads them, so the previous call's contents in
   // the shared array need no clearing.
   attn::BuildLaunch b;
   b.slices = t.slices;
+  b.qb_ptr = reinterpret_cast<const int32_t *>(ws + L.qb_ptr);
+  b.qb_idx = reinterpret_cast<const int32_t *>(ws + L.qb_idx);
   b.n_slices = n_slices;
   b.sq = sq;
   b.sk = sk;

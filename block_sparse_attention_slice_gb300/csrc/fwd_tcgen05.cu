@@ -10,8 +10,11 @@
 // (FlashAttention-4 page, "conditional softmax rescaling"); the final
 // O = o / l uses the same reference, so the result is exact either way.
 //
-// Persistent kernel: one CTA per SM walks the work items (query tile, head)
-// in longest-processing-time order with a static stride.  A work item is 256
+// Persistent kernel: one CTA per SM takes work items (query tile, head) in
+// longest-processing-time order from a global counter (the producer lane
+// fetches and publishes each item id to the CTA's other roles through a
+// small shared-memory queue), so the CTAs finish together and the next
+// item's Q load and first QK overlap the previous item's epilogue.  A work item is 256
 // query rows of one head (two 128-row MMA tiles, t = 0, 1) against the
 // KV-tile list of that 256-row query tile.  Warp roles (352 threads):
 //   warps 0-3  softmax of tile 0 (thread = row = tensor-memory lane)
@@ -36,8 +39,10 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "attn_internal.h"
 #include "ptx.cuh"
@@ -51,6 +56,12 @@ constexpr int BN = 128;           // keys per KV tile
 constexpr float TAU = 8.0f;       // lazy-rescale threshold, log2 units
 constexpr int NTHREADS = 352;
 constexpr int RING = 32;          // metadata records in flight
+constexpr int IQ = 4;             // queued work-item ids
+constexpr int SCHED_SLOTS = 4096; // work counters, one per launch in flight
+
+// Work counters of forward launches: each launch takes the next slot (host
+// side, round robin) and zeroes it on its stream before the kernel runs.
+__device__ unsigned int g_sched_counter[SCHED_SLOTS];
 
 struct FwdParams {
   const int32_t *row_ptr, *col_idx, *ref_ptr, *ref_idx, *sched;
@@ -62,6 +73,7 @@ struct FwdParams {
   int out_f32;
   float scale_log2;               // scale * log2(e)
   unsigned long long wait_ns;
+  unsigned int *counter;          // this launch's work counter (zeroed before launch)
 };
 
 // One resolved tile entry: key tile, kind, reference range and up to two
@@ -81,12 +93,14 @@ struct Layout {
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TILE;
   static constexpr int REC_OFF = KV_OFF + NS * TILE;
-  static constexpr int BAR_OFF = REC_OFF + RING * 64;
+  static constexpr int IQ_OFF = REC_OFF + RING * 64;
+  static constexpr int BAR_OFF = IQ_OFF + IQ * 16;
   // q_full | q_empty | full[NS] | empty[NS] | s_full[2] | p_full[2] | o_full[2] | drain |
-  // rec_full[RING] | rec_empty[RING]
+  // rec_full[RING] | rec_empty[RING] | iq_full[IQ] | iq_empty[IQ]
   static constexpr int B_Q = 0, B_QE = 1, B_FULL = 2, B_EMPTY = 2 + NS, B_S = 2 + 2 * NS,
                        B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2, B_RF = B_DRAIN + 1,
-                       B_RE = B_RF + RING, NBAR = B_RE + RING;
+                       B_RE = B_RF + RING, B_IF = B_RE + RING, B_IE = B_IF + IQ,
+                       NBAR = B_IE + IQ;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;
@@ -175,6 +189,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
   Rec *recs = reinterpret_cast<Rec *>(smem + L::REC_OFF);
+  volatile int *iq = reinterpret_cast<volatile int *>(smem + L::IQ_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_ns;
@@ -197,6 +212,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(L::B_RF + r), 1);
       mbar_init(bar(L::B_RE + r), 8);
     }
+    // item ids are read by the MMA lane, the metadata warp and 8 softmax warps
+    for (int u = 0; u < IQ; ++u) {
+      mbar_init(bar(L::B_IF + u), 1);
+      mbar_init(bar(L::B_IE + u), 10);
+    }
     *abort = 0;
     fence_mbar_init();
   }
@@ -217,9 +237,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t ld = 0, nonempty = 0;
+      uint32_t ld = 0, nonempty = 0, qpos = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      while (ok) {
+        // fetch the next item and publish it to the other roles
+        const int qs = qpos % IQ;
+        if (qpos >= IQ && !mbar_wait_bounded(bar(L::B_IE + qs), (qpos / IQ - 1) & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        const int item = static_cast<int>(atomicAdd(p.counter, 1u));
+        iq[qs] = item;
+        mbar_arrive(bar(L::B_IF + qs));
+        ++qpos;
+        if (item >= p.n_items) break;
         const Item it = decode(p, item);
         if (it.n == 0) continue;
         if (nonempty > 0 && !mbar_wait_bounded(bar(L::B_QE), (nonempty - 1) & 1, abort, lim)) {
@@ -284,7 +315,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       };
       uint32_t ld = 0, nonempty = 0, step = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      uint32_t qpos = 0;
+      while (ok) {
+        const int qs = qpos % IQ;
+        if (!mbar_wait_bounded(bar(L::B_IF + qs), (qpos / IQ) & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        const int item = iq[qs];
+        mbar_arrive(bar(L::B_IE + qs));
+        ++qpos;
+        if (item >= p.n_items) break;
         const Item it = decode(p, item);
         const int n = it.n;
         if (n == 0) continue;
@@ -346,35 +387,50 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------------ metadata
     uint32_t rpos = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+    uint32_t qpos = 0;
+    while (ok) {
+      const int qs = qpos % IQ;
+      if (!wait_all(bar(L::B_IF + qs), (qpos / IQ) & 1, abort, lim)) {
+        ok = false;
+        break;
+      }
+      const int item = iq[qs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_IE + qs));
+      ++qpos;
+      if (item >= p.n_items) break;
       const Item it = decode(p, item);
-      for (int base = 0; base < it.n; base += 32) {
-        const int j = base + lane;
+      for (int base = 0; ok && base < it.n; base += 32) {
+        const int j = base + lane, cnt = min(32, it.n - base);
+        Rec r;
+        r.kt = r.kind = r.r0 = r.r1 = r.pad[0] = r.pad[1] = 0;
+        r.s[0] = attn_slice_t{0, 0, 0, 0, 0};
+        r.s[1] = attn_slice_t{0, 0, 0, 0, 0};
         if (j < it.n) {
           const int e = it.e0 + j;
-          Rec r;
           r.kt = __ldg(p.col_idx + e);
           r.kind = __ldg(p.kind + e);
           r.r0 = __ldg(p.ref_ptr + e);
           r.r1 = __ldg(p.ref_ptr + e + 1);
-          r.pad[0] = r.pad[1] = 0;
-          r.s[0] = attn_slice_t{0, 0, 0, 0, 0};
-          r.s[1] = attn_slice_t{0, 0, 0, 0, 0};
           if (r.r1 > r.r0) r.s[0] = p.slices[__ldg(p.ref_idx + r.r0)];
           if (r.r1 > r.r0 + 1) r.s[1] = p.slices[__ldg(p.ref_idx + r.r0 + 1)];
-          const uint32_t pos = rpos + lane;
-          const int slot = pos % RING;
-          if (pos >= RING &&
-              !mbar_wait_bounded(bar(L::B_RE + slot), (pos / RING - 1) & 1, abort, lim)) {
+        }
+        // records go out in order; lane 0 alone waits for each slot to be
+        // released (the others park at the shuffle), then lane l writes
+        for (int l = 0; l < cnt; ++l, ++rpos) {
+          const int slot = rpos % RING;
+          bool free_ok = true;
+          if (lane == 0 && rpos >= RING)
+            free_ok = mbar_wait_bounded(bar(L::B_RE + slot), (rpos / RING - 1) & 1, abort, lim);
+          if (!__shfl_sync(0xffffffffu, free_ok ? 1 : 0, 0)) {
             ok = false;
-          } else {
+            break;
+          }
+          if (lane == l) {
             recs[slot] = r;
             mbar_arrive(bar(L::B_RF + slot));
           }
         }
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        rpos += min(32, it.n - base);
       }
     }
   } else {
@@ -386,7 +442,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float sl2 = p.scale_log2;
     uint32_t step = 0, rpos = 0, nonempty = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+    uint32_t qpos = 0;
+    while (ok) {
+      const int qs = qpos % IQ;
+      if (!wait_all(bar(L::B_IF + qs), (qpos / IQ) & 1, abort, lim)) {
+        ok = false;
+        break;
+      }
+      const int item = iq[qs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_IE + qs));
+      ++qpos;
+      if (item >= p.n_items) break;
       const Item it = decode(p, item);
       const int row = it.qt * 256 + t * BM + wl * 32 + lane;
       const bool live = row < p.sq;
@@ -435,14 +502,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int k = 0; k < BN; ++k)
             if (!((w[k >> 5] >> (k & 31)) & 1u)) s[k] = -INFINITY;
         }
-        // row max as a tree: eight independent partial maxima
-        float m8[8];
+        // row max: four independent chains of three-input maxima, seeded
+        // with s[0..7] and covering s[8..BN) in rounds of eight
+        static_assert(BN % 8 == 0, "row max rounds");
+        float m4[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) m8[u] = s[u];
+        for (int u = 0; u < 4; ++u) m4[u] = fmaxf(s[2 * u], s[2 * u + 1]);
 #pragma unroll
-        for (int k = 8; k < BN; ++k) m8[k & 7] = fmaxf(m8[k & 7], s[k]);
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int k = 8; k < BN; k += 8) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) m4[u] = max3f(m4[u], s[k + 2 * u], s[k + 2 * u + 1]);
+        }
+        const float mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         const float mx2 = mx * sl2;
         const float m_old = m_ref;
         const bool grow = mx2 > m_ref + TAU;
@@ -450,20 +521,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float factor = grow ? ex2_approx(m_old - m_ref) : 1.f;
         l *= factor;
         const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};     // four independent partial sums
+        // exponent arguments and row sums on f32 pairs: four independent
+        // two-wide partial sums
+        const uint64_t sc2 = f2_make(sl2, sl2), nb2 = f2_make(-mb, -mb);
+        uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * k], sl2, -mb));
-            const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * k + 1], sl2, -mb));
-            l4[k & 3] += p0 + p1;
+            float a0, a1;
+            f2_split(f2_fma(f2_make(s[c * 32 + 2 * k], s[c * 32 + 2 * k + 1]), sc2, nb2), a0, a1);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            l2[k & 3] = f2_add(l2[k & 3], f2_make(p0, p1));
             pk[k] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tS + c * 16, pk);
         }
-        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        {
+          float x0, x1;
+          f2_split(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])), x0, x1);
+          l += x0 + x1;
+        }
         const bool rescale = grow && (m_old != -INFINITY) && j > 0;
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
@@ -568,6 +647,25 @@ static int make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t ro
 
 static unsigned long long g_wait_ns = 4000000000ull;
 constexpr int kMaxDev = 64;
+static std::atomic<unsigned int> g_launch_seq{0};
+
+// Device address of this launch's work counter (g_sched_counter on the
+// current device, looked up once per device).
+static unsigned int *next_counter() {
+  static unsigned int *base[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!base[dev]) {
+      void *ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_sched_counter) != cudaSuccess) return nullptr;
+      base[dev] = static_cast<unsigned int *>(ptr);
+    }
+  }
+  return base[dev] + (g_launch_seq.fetch_add(1) % SCHED_SLOTS);
+}
 
 static int sm_count() {
   static int cached[kMaxDev] = {};
@@ -631,6 +729,9 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   const int sms = sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   const int grid = static_cast<int>(items < sms ? items : sms);
+  p.counter = next_counter();
+  if (!p.counter || cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   if (d == 128) return launch_fwd<128, 4>(mq, mk, mv, p, grid, stream);
   return launch_fwd<64, 8>(mq, mk, mv, p, grid, stream);
 }
