@@ -28,19 +28,35 @@ int check_slices(const attn_slice_t *s, int n, int sq, int sk) {
 }
 
 // Rectangles of non-empty slices must be pairwise disjoint.  Sorted by
-// q_start, a slice can only meet the following ones that start before it
-// ends in q.
+// (q_start, k_start), a slice can only meet the following ones that start
+// before it ends in q; within a run of equal q_start, once a k_start reaches
+// its k_end the rest of the run is past it too, so the scan skips to the
+// next run.  Lists that come sorted (block grids, most slice lists) skip the
+// sort, and a grid is checked in linear time.
 int check_overlap(const attn_slice_t *s, int n) {
   std::vector<int> idx;
   idx.reserve(n);
   for (int i = 0; i < n; ++i)
     if (s[i].q_end > s[i].q_start && s[i].k_end > s[i].k_start) idx.push_back(i);
-  std::sort(idx.begin(), idx.end(), [&](int a, int b) { return s[a].q_start < s[b].q_start; });
-  for (size_t u = 0; u < idx.size(); ++u) {
+  auto before = [&](int a, int b) {
+    return s[a].q_start != s[b].q_start ? s[a].q_start < s[b].q_start : s[a].k_start < s[b].k_start;
+  };
+  if (!std::is_sorted(idx.begin(), idx.end(), before)) std::sort(idx.begin(), idx.end(), before);
+  const size_t m = idx.size();
+  std::vector<size_t> run_end(m);
+  for (size_t u = m; u-- > 0;)
+    run_end[u] = (u + 1 < m && s[idx[u + 1]].q_start == s[idx[u]].q_start) ? run_end[u + 1] : u + 1;
+  for (size_t u = 0; u < m; ++u) {
     const attn_slice_t &a = s[idx[u]];
-    for (size_t v = u + 1; v < idx.size() && s[idx[v]].q_start < a.q_end; ++v) {
+    size_t v = u + 1;
+    while (v < m && s[idx[v]].q_start < a.q_end) {
       const attn_slice_t &b = s[idx[v]];
+      if (b.q_start == a.q_start && b.k_start >= a.k_end) {
+        v = run_end[v];
+        continue;
+      }
       if (a.k_start < b.k_end && b.k_start < a.k_end) return ATTN_ERR_OVERLAP;
+      ++v;
     }
   }
   return ATTN_OK;

@@ -20,13 +20,15 @@
 //          argument checks: ids of the slices meeting its rows, ascending)
 //   fill   one CTA per query tile: its offsets (sums over the preceding
 //          query tiles), recount, compact the entries in ascending key-tile
-//          order, write the ascending slice references, and place the query
-//          tile at its rank of the longest-processing-time order; CTA 0 also
-//          writes the totals
-// Counting is warp-parallel over the rows of a (slice, key tile) pair and
-// visits only the key tiles a slice can touch inside the query tile: for
-// every slice kind the row interval's ends never decrease with the row, so
-// the first row's start and the last row's end bound them.
+//          order, write the ascending slice references (one warp per masked
+//          key tile), and place the query tile at its rank of the
+//          longest-processing-time order; CTA 0 also writes the totals
+// For every slice kind the row interval's ends never decrease with the row,
+// so the first row's start and the last row's end bound the key tiles a
+// slice can touch inside a query tile, and decide in O(1) the tiles it
+// covers or misses entirely; only tiles cut by an interval end are counted
+// row by row, lane-parallel.  Warps take one slice each when a query tile
+// has many, or split one slice's key tiles when it has few.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -61,6 +63,22 @@ __device__ __forceinline__ int warp_pairs_in(const attn_slice_t &s, int r0, int 
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
   return c;
+}
+
+// Same count, exact in O(1) when every row of the slice inside [r0, r1)
+// covers [c0, c1) or misses it: the row interval's ends never decrease with
+// the row, so the first and last rows bound all of them.  Only tiles cut by
+// an interval end fall back to the row loop.
+__device__ __forceinline__ int warp_pairs_fast(const attn_slice_t &s, int r0, int r1, int c0,
+                                               int c1, int lane) {
+  const int a = max(r0, s.q_start), b = min(r1, s.q_end);
+  if (a >= b) return 0;
+  int lo_a, hi_a, lo_b, hi_b;
+  row_interval(s, a, lo_a, hi_a);
+  row_interval(s, b - 1, lo_b, hi_b);
+  if (hi_b <= c0 || lo_a >= c1) return 0;
+  if (lo_b <= c0 && hi_a >= c1) return (b - a) * (c1 - c0);
+  return warp_pairs_in(s, r0, r1, c0, c1, lane);
 }
 
 // Key tiles [*kt0, *kt1] that slice s can touch within rows [r0, r1); empty
@@ -115,22 +133,35 @@ __device__ int block_excl_scan(int v, int *sh, int *total) {
 __device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref) {
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NW = BT / 32;
   for (int t = threadIdx.x; t < b.nk; t += BT) {
     cnt[t] = 0;
     nref[t] = 0;
   }
   __syncthreads();
   const int u0 = b.qb_ptr[qt], u1 = b.qb_ptr[qt + 1];
-  for (int u = u0; u < u1; ++u) {
-    const attn_slice_t s = b.slices[b.qb_idx[u]];
-    int kt0, kt1;
-    touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
-    for (int kt = kt0 + warp; kt <= kt1; kt += BT / 32) {
-      const int c = warp_pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane);
-      if (c > 0 && lane == 0) {
-        atomicAdd(&cnt[kt], c);
-        atomicAdd(&nref[kt], 1);
-      }
+  auto tally = [&](const attn_slice_t &s, int kt) {
+    const int c = warp_pairs_fast(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane);
+    if (c > 0 && lane == 0) {
+      atomicAdd(&cnt[kt], c);
+      atomicAdd(&nref[kt], 1);
+    }
+  };
+  if (u1 - u0 < NW) {
+    // few slices: the warps split each slice's key tiles
+    for (int u = u0; u < u1; ++u) {
+      const attn_slice_t s = b.slices[b.qb_idx[u]];
+      int kt0, kt1;
+      touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
+      for (int kt = kt0 + warp; kt <= kt1; kt += NW) tally(s, kt);
+    }
+  } else {
+    // many slices: one warp per slice
+    for (int u = u0 + warp; u < u1; u += NW) {
+      const attn_slice_t s = b.slices[b.qb_idx[u]];
+      int kt0, kt1;
+      touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
+      for (int kt = kt0; kt <= kt1; ++kt) tally(s, kt);
     }
   }
   __syncthreads();
@@ -255,20 +286,24 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
   __syncthreads();
   // slice references of MASKED tiles, ascending slice id: slices are visited
   // in ascending order and each key tile is written by one thread per slice
+  // slice references of MASKED tiles: one warp per key tile walks the
+  // bucket in ascending slice id, so each list comes out ordered
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u0 = b.qb_ptr[qt], u1 = b.qb_ptr[qt + 1];
-  for (int u = u0; u < u1; ++u) {
-    const int sid = b.qb_idx[u];
-    const attn_slice_t s = b.slices[sid];
-    int kt0, kt1;
-    touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
-    for (int kt = kt0 + warp; kt <= kt1; kt += BT / 32) {
-      if (cnt[kt] <= 0 || cnt[kt] == full) continue;
-      if (warp_pairs_in(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane) > 0 && lane == 0)
-        b.ref_idx[rpos[kt]++] = sid;
+  for (int kt = warp; kt < b.nk; kt += BT / 32) {
+    if (cnt[kt] <= 0 || cnt[kt] == full) continue;
+    int pos = rpos[kt];
+    const int c0 = kt * b.tk, c1 = min((kt + 1) * b.tk, b.sk);
+    for (int u = u0; u < u1; ++u) {
+      const int sid = b.qb_idx[u];
+      const attn_slice_t s = b.slices[sid];
+      if (s.k_end <= c0 || s.k_start >= c1) continue;
+      if (warp_pairs_fast(s, r0, r1, c0, c1, lane) > 0) {
+        if (lane == 0) b.ref_idx[pos] = sid;
+        ++pos;
+      }
     }
-    __syncthreads();
   }
 }
 

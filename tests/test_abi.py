@@ -73,3 +73,32 @@ def test_workspace_bound_and_argument_checks(lib):
                               ctypes.byref(st), None)
     assert rc == B.ATTN_ERR_OVERLAP
     assert lib.attn_strerror(B.ATTN_ERR_TIMEOUT).decode().startswith("a bounded")
+
+
+def _brute_overlap(sl):
+    r = [x for x in sl.tolist() if x[1] > x[0] and x[3] > x[2]]
+    for i in range(len(r)):
+        for j in range(i + 1, len(r)):
+            a, b = r[i], r[j]
+            if a[0] < b[1] and b[0] < a[1] and a[2] < b[3] and b[2] < a[3]:
+                return True
+    return False
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_planted_overlaps_are_found_before_any_device_work(lib, seed):
+    # a disjoint random list plus one slice overlapping a random member; the
+    # host check must reject it before anything reaches the device
+    rng = np.random.default_rng(seed)
+    base = W.random_slices(4096, 4096, 60, seed=seed, unit=16, max_len=40)
+    assert not _brute_overlap(base)
+    victim = base[rng.integers(len(base))]
+    qs = int(rng.integers(victim[0], victim[1])); ks = int(rng.integers(victim[2], victim[3]))
+    extra = np.array([[qs, min(4096, qs + 5), ks, min(4096, ks + 7), int(rng.integers(4))]], np.int32)
+    sl = np.concatenate([base, extra])[rng.permutation(len(base) + 1)]
+    assert _brute_overlap(sl)
+    arr, cnt = B._slice_array(sl)
+    st = B.AttnTiles()
+    rc = lib.attn_build_tiles(arr, cnt, 4096, 4096, 256, 128, ctypes.c_void_p(256), 1 << 30,
+                              ctypes.byref(st), None)
+    assert rc == B.ATTN_ERR_OVERLAP

@@ -65,3 +65,25 @@ def test_bounded_wait_times_out_and_reports():
     torch.cuda.synchronize()
     assert attn_last_device_error() == 0
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_overlap_check_agrees_with_brute_force(seed):
+    from block_sparse_attention_slice_gb300 import workloads as W
+    rng = np.random.default_rng(seed + 50)
+    for trial in range(6):
+        sl = W.random_slices(2048, 2048, 40, seed=seed * 10 + trial, unit=8, max_len=30)
+        if trial % 2:
+            v = sl[rng.integers(len(sl))]
+            q0 = min(2039, int(rng.integers(max(0, v[0] - 8), v[1])))
+            k0 = min(2039, int(rng.integers(max(0, v[2] - 8), v[3])))
+            sl = np.concatenate([sl, np.array([[q0, q0 + 9, k0, k0 + 9, 0]], np.int32)])
+        rows = [x for x in sl.tolist() if x[1] > x[0] and x[3] > x[2]]
+        expect = any(a[0] < b[1] and b[0] < a[1] and a[2] < b[3] and b[2] < a[3]
+                     for i, a in enumerate(rows) for b in rows[i + 1:])
+        if expect:
+            with pytest.raises(AttnError) as e:
+                attn_build_tiles(sl, 2048, 2048)
+            assert e.value.code == B.ATTN_ERR_OVERLAP
+        else:
+            attn_build_tiles(sl, 2048, 2048).to_host()
