@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="varlen_causal")
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                    help="fwd: the forward hot path (default); bwd: attn_bwd alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -441,11 +443,72 @@ def gpu_arm(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def bwd_arm(args, ws, rank, local):
+    """attn_bwd on one workload, inputs and forward results resident: valid
+    pairs x 10 d FLOPs (2.5 x the forward's 4 d, the usual count for five
+    GEMMs) per second of attn_bwd time."""
+    import torch
+
+    import block_sparse_attention_slice_gb300 as pkg
+    from block_sparse_attention_slice_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.load()
+    w = W.ALL[args.workload]()
+    sl = slices_of(w)
+    q, k, v = W.draw_qkv(w.S, w.H, w.Hk, w.d, w.seed)
+    rng = np.random.default_rng(w.seed + 1)
+    do = torch.from_numpy(rng.standard_normal((w.S, w.H, w.d), dtype=np.float32)).to(torch.bfloat16)
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    tiles = pkg.attn_build_tiles(sl, w.S, w.S)
+    pairs = tiles.totals()[2]
+    out, lse = pkg.attn_fwd(qd, kd, vd, tiles, w.scale)
+    wsb = None
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    steps = args.steps if args.steps is not None else 10
+    for _ in range(max(3, args.warmup)):
+        pkg.attn_bwd(qd, kd, vd, out, dod, lse, tiles, w.scale, grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    clocks = Clocks(local) if rank == 0 else None
+    barrier(ws)
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.zero_()
+        a.record()
+        pkg.attn_bwd(qd, kd, vd, out, dod, lse, tiles, w.scale, grad_dtype=torch.bfloat16)
+        b.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop() if clocks else None
+    if pkg.attn_last_device_error() != 0:
+        raise RuntimeError("device status after the timed region")
+    ms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in evs), ws, dev)
+    flops = 10.0 * w.d * pairs * w.H
+    pk, pk_src = peaks()
+    val = flops / (ms / 1e3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": "masked attn bwd TFLOPS (valid-pair, 2.5x forward FLOPs) and % of GB300 BF16 dense peak",
+            "value": ws * val, "unit": "TFLOP/s", "n_gpus": ws, "steps": steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "S": w.S, "H": w.H, "Hk": w.Hk, "d": w.d,
+                       "valid_pairs_per_head": pairs, "l2": "flushed between timed steps"},
+            "roofline": {"kernel": "attn_bwd", "bound": "tensor", "achieved": val,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": val / pk["bf16_tflops"],
+                         "traffic": None, "peak_source": f"bf16_tflops (burst) of {pk_src}"},
+            "gpu_launches": 6 * steps, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_init()
     if args.impl == "reference":
         reference_arm(args, ws, rank)
+    elif args.which == "bwd":
+        bwd_arm(args, ws, rank, local)
     else:
         gpu_arm(args, ws, rank, local)
     if ws > 1:

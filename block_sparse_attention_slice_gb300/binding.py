@@ -25,7 +25,8 @@ ATTN_MERGE_MAX_PARTS = 16
 # every entry point declared in include/attn_slice.h
 EXPORTS = ["attn_tiles_workspace_bytes", "attn_build_tiles", "attn_build_tiles_noalloc",
            "attn_tiles_totals",
-           "attn_slices_from_block_grid", "attn_fwd", "attn_merge", "attn_last_device_error",
+           "attn_slices_from_block_grid", "attn_fwd", "attn_merge", "attn_bwd_workspace_bytes",
+           "attn_bwd", "attn_last_device_error",
            "attn_set_wait_limit_ns", "attn_selftest_wait_timeout", "attn_strerror"]
 
 
@@ -75,6 +76,9 @@ def load(path: Optional[str] = None):
     lib.attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
                              ctypes.POINTER(AttnTiles), vp, i32, vp, vp]
     lib.attn_merge.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp]
+    lib.attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(AttnTiles), i32, ctypes.POINTER(sz)]
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
+                             ctypes.POINTER(AttnTiles), vp, vp, vp, i32, vp, sz, vp]
     lib.attn_last_device_error.argtypes = [vp]
     lib.attn_set_wait_limit_ns.argtypes = [i64]
     lib.attn_selftest_wait_timeout.argtypes = [vp]
@@ -266,6 +270,33 @@ def attn_merge(o_parts: Sequence, lse_parts: Sequence, out=None, lse=None, out_d
     _check(load().attn_merge(optr, lptr, n, pd, S, H, d, out.data_ptr(), od, lse.data_ptr(),
                              _stream_ptr(stream)), "attn_merge")
     return out, lse
+
+
+def attn_bwd(q, k, v, out, dout, lse, tiles: Tiles, scale: float, grad_dtype=None, ws=None,
+             stream=None):
+    """dQ, dK, dV of the masked attention forward (dout bf16 like q)."""
+    import torch
+    sq, hq, d = q.shape
+    sk, hk, _ = k.shape
+    for x in (q, k, v, dout):
+        if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+            raise ValueError("q, k, v, dout must be contiguous bf16 CUDA tensors")
+    gd = grad_dtype or torch.float32
+    dq = torch.empty((sq, hq, d), dtype=gd, device=q.device)
+    dk = torch.empty((sk, hk, d), dtype=gd, device=q.device)
+    dv = torch.empty((sk, hk, d), dtype=gd, device=q.device)
+    nb = ctypes.c_size_t(0)
+    _check(load().attn_bwd_workspace_bytes(ctypes.byref(tiles.struct), hq, ctypes.byref(nb)),
+           "attn_bwd_workspace_bytes")
+    if ws is None or ws.numel() < nb.value:
+        ws = torch.empty(int(nb.value), dtype=torch.uint8, device=q.device)
+    od = ATTN_DTYPE_F32 if out.dtype == torch.float32 else ATTN_DTYPE_BF16
+    gc = ATTN_DTYPE_F32 if gd == torch.float32 else ATTN_DTYPE_BF16
+    _check(load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), od, dout.data_ptr(),
+                           lse.data_ptr(), sq, sk, hq, hk, d, float(scale), ctypes.byref(tiles.struct),
+                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), gc, ctypes.c_void_p(ws.data_ptr()),
+                           ws.numel(), _stream_ptr(stream)), "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_last_device_error(stream=None) -> int:

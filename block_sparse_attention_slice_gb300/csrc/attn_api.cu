@@ -273,6 +273,35 @@ int attn_fwd(const void *q, const void *k, const void *v, int sq, int sk, int hq
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
+int attn_bwd_workspace_bytes(const attn_tiles_t *tiles, int hq, size_t *bytes) {
+  if (!tiles || !bytes || hq < 1 || !tiles->row_ptr) return ATTN_ERR_INVALID_ARG;
+  *bytes = attn::bwd_workspace_bytes(tiles->sq, hq, tiles->n_ktiles, tiles->cap_entries);
+  return ATTN_OK;
+}
+
+int attn_bwd(const void *q, const void *k, const void *v, const void *out, int out_dtype,
+             const void *dout, const float *lse, int sq, int sk, int hq, int hk, int d, float scale,
+             const attn_tiles_t *tiles, void *dq, void *dk, void *dv, int grad_dtype, void *d_ws,
+             size_t ws_bytes, attn_stream_t stream) {
+  if (!q || !k || !v || !out || !dout || !lse || !tiles || !dq || !dk || !dv || !d_ws)
+    return ATTN_ERR_INVALID_ARG;
+  if (sq < 1 || sk < 1 || hq < 1 || hk < 1 || hq % hk != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if ((out_dtype != ATTN_DTYPE_BF16 && out_dtype != ATTN_DTYPE_F32) ||
+      (grad_dtype != ATTN_DTYPE_BF16 && grad_dtype != ATTN_DTYPE_F32))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (tiles->sq != sq || tiles->sk != sk || !tiles->row_ptr) return ATTN_ERR_INVALID_ARG;
+  if (tiles->tile_q != ATTN_FWD_TILE_Q || tiles->tile_k != ATTN_FWD_TILE_K) return ATTN_ERR_UNSUPPORTED;
+  const void *ptrs[] = {q, k, v, out, dout, dq, dk, dv, d_ws};
+  for (const void *ptr : ptrs)
+    if (!aligned16(ptr)) return ATTN_ERR_UNSUPPORTED;
+  if (ws_bytes < attn::bwd_workspace_bytes(sq, hq, tiles->n_ktiles, tiles->cap_entries))
+    return ATTN_ERR_CAPACITY;
+  return attn::bwd_launch(q, k, v, out, out_dtype, dout, lse, sq, sk, hq, hk, d, scale, tiles, dq, dk,
+                          dv, grad_dtype, d_ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int attn_merge(const void *const *h_o_parts, const float *const *h_lse_parts, int n_parts,
                int part_dtype, int s_len, int h, int d, void *out, int out_dtype, float *lse,
                attn_stream_t stream) {
@@ -297,9 +326,10 @@ int attn_merge(const void *const *h_o_parts, const float *const *h_lse_parts, in
 int attn_last_device_error(attn_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  unsigned int st = 0;
-  if (attn::fwd_status_take(&st) != ATTN_OK) return ATTN_ERR_CUDA;
-  return st ? ATTN_ERR_TIMEOUT : ATTN_OK;
+  unsigned int st = 0, sb = 0;
+  if (attn::fwd_status_take(&st) != ATTN_OK || attn::bwd_status_take(&sb) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  return (st || sb) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 int attn_set_wait_limit_ns(int64_t ns) {

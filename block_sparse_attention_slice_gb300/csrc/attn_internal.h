@@ -47,7 +47,15 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
                cudaStream_t stream);
 int fwd_status_take(unsigned int *status);
 void fwd_set_wait_ns(unsigned long long ns);
+unsigned long long wait_limit_ns();
 int selftest_timeout_launch(cudaStream_t s);
+
+size_t bwd_workspace_bytes(int sq, int hq, int n_ktiles, int64_t cap_entries);
+int bwd_launch(const void *q, const void *k, const void *v, const void *out, int out_dtype,
+               const void *dout, const float *lse, int sq, int sk, int hq, int hk, int d, float scale,
+               const attn_tiles_t *tiles, void *dq, void *dk, void *dv, int grad_dtype, void *d_ws,
+               cudaStream_t stream);
+int bwd_status_take(unsigned int *status);
 
 int merge_launch(const void *const *o_parts, const float *const *lse_parts, int n_parts,
                  int part_dtype, int s_len, int h, int d, void *out, int out_dtype, float *lse,

@@ -1,0 +1,772 @@
+// Backward pass of masked attention on sm_103a: dQ, dK, dV from Q, K, V, the
+// forward output O and its LSE, and the output gradient dO, for the same
+// slice masks and tile metadata as the forward.
+//
+// With P = softmax(scale Q K^T + mask) recomputed from the saved LSE:
+//   D   = rowsum(dO * O)                       (bwd_delta_kernel)
+//   dP  = dO V^T,  dS = P * (dP - D)
+//   dV  = P^T dO,  dK = scale dS^T Q            (bwd_kv_kernel, per key tile)
+//   dQ  = scale dS K                            (bwd_q_kernel, per query tile)
+// The key-tile kernel walks a transposed copy of the CSR tile lists (per
+// key tile: the query tiles that have it, ascending), built deterministically
+// by csc_count_kernel / csc_fill_kernel; dK and dV of a key tile accumulate
+// in tensor memory over every query tile and every query head of its GQA
+// group, so each is written once.  dQ is computed by a second walk of the
+// forward's per-query-tile lists, so no kernel needs atomics.
+//
+// All MMAs have the forward's two forms: S^T = K Q^T and dP^T = V dO^T (both
+// operands K-major in shared memory), dV += P^T dO and dK += dS^T Q (A read
+// from tensor memory, B MN-major in shared memory); likewise S = Q K^T,
+// dP = dO V^T and dQ += dS K in the query-tile kernel.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_device.cuh"
+#include "attn_internal.h"
+
+namespace attn {
+
+__device__ unsigned int g_bwd_status;
+
+constexpr int B_THREADS = 192;     // warps 0-3 element-wise, 4 producer, 5 MMA issuer
+constexpr int B_TILE_Q = 256;      // query rows per tile of the metadata
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct BwdParams {
+  const int32_t *row_ptr, *col_idx, *ref_ptr, *ref_idx, *sched;
+  const uint8_t *kind;
+  const attn_slice_t *slices;
+  const int32_t *col_ptr, *col_q, *col_e, *col_sched;
+  const float *lse, *delta;
+  void *dq, *dk, *dv;
+  int sq, sk, hq, hk, n_qtiles, n_ktiles;
+  int grad_f32;
+  float scale, scale_log2;
+  unsigned long long wait_ns;
+};
+
+// ------------------------------------------------------------------ D = rowsum(dO * O)
+template <int D, bool O_F32>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const void *out, const uint16_t *dout,
+                                                         float *delta, int sq, int hq) {
+  constexpr int V = D / 32;
+  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= static_cast<long long>(sq) * hq) return;
+  const int h = static_cast<int>(w / sq), i = static_cast<int>(w % sq);
+  const size_t base = (static_cast<size_t>(i) * hq + h) * D + lane * V;
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const float g = __uint_as_float(static_cast<uint32_t>(dout[base + k]) << 16);
+    const float o = O_F32 ? static_cast<const float *>(out)[base + k]
+                          : __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(out)[base + k]) << 16);
+    acc = fmaf(g, o, acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) delta[static_cast<size_t>(h) * sq + i] = acc;
+}
+
+// ------------------------------------------------------------------ transposed lists
+// Position of key tile kt in query tile qt's sorted list, or -1.
+__device__ __forceinline__ int find_entry(const BwdParams &p, int qt, int kt) {
+  int lo = p.row_ptr[qt], hi = p.row_ptr[qt + 1];
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const int c = p.col_idx[mid];
+    if (c == kt) return mid;
+    if (c < kt) lo = mid + 1; else hi = mid;
+  }
+  return -1;
+}
+
+__device__ long long block_sum_ll(long long v, long long *red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  long long t = 0;
+  for (int u = 0; u < static_cast<int>(blockDim.x >> 5); ++u) t += red[u];
+  return t;
+}
+
+__global__ void __launch_bounds__(256) csc_count_kernel(BwdParams p, int32_t *colcnt) {
+  __shared__ long long red[8];
+  const int kt = blockIdx.x;
+  long long c = 0;
+  for (int qt = threadIdx.x; qt < p.n_qtiles; qt += blockDim.x) c += find_entry(p, qt, kt) >= 0;
+  c = block_sum_ll(c, red);
+  if (threadIdx.x == 0) colcnt[kt] = static_cast<int32_t>(c);
+}
+
+__global__ void __launch_bounds__(256) csc_fill_kernel(BwdParams p, const int32_t *colcnt,
+                                                       int32_t *col_ptr, int32_t *col_q,
+                                                       int32_t *col_e, int32_t *col_sched) {
+  __shared__ long long red[8];
+  __shared__ int scan[256];
+  const int kt = blockIdx.x, me = colcnt[kt];
+  long long before = 0, all = 0, rank = 0;
+  for (int u = threadIdx.x; u < p.n_ktiles; u += blockDim.x) {
+    const int cu = colcnt[u];
+    if (u < kt) before += cu;
+    all += cu;
+    rank += (cu > me || (cu == me && u < kt)) ? 1 : 0;
+  }
+  before = block_sum_ll(before, red);
+  all = block_sum_ll(all, red);
+  rank = block_sum_ll(rank, red);
+  if (threadIdx.x == 0) {
+    col_ptr[kt] = static_cast<int32_t>(before);
+    col_sched[rank] = kt;
+    if (kt == 0) col_ptr[p.n_ktiles] = static_cast<int32_t>(all);
+  }
+  // ascending query tiles, 256 at a time
+  int out = static_cast<int>(before);
+  for (int base = 0; base < p.n_qtiles; base += blockDim.x) {
+    const int qt = base + threadIdx.x;
+    const int e = qt < p.n_qtiles ? find_entry(p, qt, kt) : -1;
+    scan[threadIdx.x] = e >= 0;
+    __syncthreads();
+    for (int o = 1; o < static_cast<int>(blockDim.x); o <<= 1) {
+      const int v = threadIdx.x >= static_cast<unsigned>(o) ? scan[threadIdx.x - o] : 0;
+      __syncthreads();
+      scan[threadIdx.x] += v;
+      __syncthreads();
+    }
+    if (e >= 0) {
+      const int pos = out + scan[threadIdx.x] - 1;
+      col_q[pos] = qt;
+      col_e[pos] = e;
+    }
+    out += scan[blockDim.x - 1];
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ shared pieces
+template <int D>
+struct BLayout {
+  static constexpr int HALF = 128 * 64 * 2;
+  static constexpr int NHALF = D / 64;
+  static constexpr int TILE = NHALF * HALF;
+};
+
+// The element-wise step shared by both kernels: from S (scores, f32) and dP
+// in tensor memory, P = exp2(S scale log2e - lse2) on the valid columns and
+// dS = P (dP - D); dS (and P when p_col >= 0) go back to tensor memory as
+// bf16 pairs.  lse2 / dlt give the per-column (kv kernel) or per-row (q
+// kernel) statistics through the callables.
+template <typename LSE, typename DLT>
+__device__ __forceinline__ void p_ds_step(uint32_t t_s, uint32_t t_dp, int p_col, int ds_col,
+                                          const uint32_t (&w)[4], float sl2, LSE lse2, DLT dlt) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t x[32], y[32];
+    tmem_ld32(t_s + c * 32, x);
+    tmem_ld32(t_dp + c * 32, y);
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      asm volatile("" : "+r"(x[k]));
+      asm volatile("" : "+r"(y[k]));
+    }
+    uint32_t pk[16], dk[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      float pv[2], dv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int col = c * 32 + 2 * k + u;
+        const bool ok = (w[col >> 5] >> (col & 31)) & 1u;
+        const float e = ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), sl2, -lse2(col)));
+        pv[u] = ok ? e : 0.f;
+        dv[u] = pv[u] * (__uint_as_float(y[2 * k + u]) - dlt(col));
+      }
+      pk[k] = pack_bf16x2(pv[0], pv[1]);
+      dk[k] = pack_bf16x2(dv[0], dv[1]);
+    }
+    if (p_col >= 0) tmem_st16(t_s + p_col + c * 16, pk);
+    tmem_st16(t_s + ds_col + c * 16, dk);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void store_rows(void *base_ptr, bool f32, size_t off, const uint32_t (&r)[32],
+                                           float mul) {
+  if (f32) {
+    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(base_ptr) + off);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      dst[k] = make_float4(__uint_as_float(r[4 * k]) * mul, __uint_as_float(r[4 * k + 1]) * mul,
+                           __uint_as_float(r[4 * k + 2]) * mul, __uint_as_float(r[4 * k + 3]) * mul);
+  } else {
+    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base_ptr) + off);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 v;
+      v.x = pack_bf16x2(__uint_as_float(r[8 * k + 0]) * mul, __uint_as_float(r[8 * k + 1]) * mul);
+      v.y = pack_bf16x2(__uint_as_float(r[8 * k + 2]) * mul, __uint_as_float(r[8 * k + 3]) * mul);
+      v.z = pack_bf16x2(__uint_as_float(r[8 * k + 4]) * mul, __uint_as_float(r[8 * k + 5]) * mul);
+      v.w = pack_bf16x2(__uint_as_float(r[8 * k + 6]) * mul, __uint_as_float(r[8 * k + 7]) * mul);
+      dst[k] = v;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV per key tile
+// Work item: (key tile kt, KV head g).  Steps: every query tile of kt's
+// column, every query head of group g, both 128-row halves.  Tensor memory:
+// S^T [0,128)  dP^T [128,256)  dV [256,256+D)  dK [384,384+D); P^T and dS^T
+// (bf16) overwrite the first 64 columns of S^T and dP^T.
+template <int D>
+struct KVLayout {
+  using B = BLayout<D>;
+  static constexpr int K_OFF = 0, V_OFF = B::TILE, ST_OFF = 2 * B::TILE;   // 2 stages of (Q, dO)
+  static constexpr int VEC_OFF = ST_OFF + 4 * B::TILE;                      // [2][lse2 128 | D 128]
+  static constexpr int BAR_OFF = VEC_OFF + 2 * 256 * 4;
+  static constexpr int B_KV = 0, B_SF = 1, B_SE = 3, B_ST = 5, B_P = 6, B_O = 7, B_DR = 8, B_VEC = 9,
+                       NBAR = 10;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int ALLOC = MISC_OFF + 16 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(B_THREADS, 1)
+    bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+  using L = KVLayout<D>;
+  using BL = BLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + L::BAR_OFF + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
+  volatile int *abort = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
+  float *vec = reinterpret_cast<float *>(smem + L::VEC_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t lim = p.wait_ns;
+
+  const int kt = p.col_sched[blockIdx.x / p.hk];
+  const int g = blockIdx.x % p.hk;
+  const int G = p.hq / p.hk;
+  const int c0 = p.col_ptr[kt], nc = p.col_ptr[kt + 1] - c0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::B_KV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::B_SF + s), 1);
+      mbar_init(bar(L::B_SE + s), 1);
+    }
+    mbar_init(bar(L::B_ST), 1);
+    mbar_init(bar(L::B_P), 128);
+    mbar_init(bar(L::B_O), 1);
+    mbar_init(bar(L::B_DR), 1);
+    mbar_init(bar(L::B_VEC), 128);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // the steps of this item: (column entry c, head offset hh, half t) with
+  // the half inside the query sequence
+  auto half_ok = [&](int c, int t) { return p.col_q[c0 + c] * B_TILE_Q + t * 128 < p.sq; };
+
+  if (warp == 4) {
+    if (lane == 0 && nc > 0) {
+      mbar_arrive_expect_tx(bar(L::B_KV), 2 * BL::TILE);
+      for (int hh = 0; hh < BL::NHALF; ++hh) {
+        tma_load_2d(sb + L::K_OFF + hh * BL::HALF, &tm_k, bar(L::B_KV), g * D + hh * 64, kt * 128);
+        tma_load_2d(sb + L::V_OFF + hh * BL::HALF, &tm_v, bar(L::B_KV), g * D + hh * 64, kt * 128);
+      }
+      uint32_t s = 0;
+      bool ok = true;
+      for (int c = 0; ok && c < nc; ++c)
+        for (int gh = 0; ok && gh < G; ++gh)
+          for (int t = 0; ok && t < 2; ++t) {
+            if (!half_ok(c, t)) continue;
+            const int st = s & 1;
+            if (s >= 2 && !mbar_wait_bounded(bar(L::B_SE + st), ((s >> 1) - 1) & 1, abort, lim)) {
+              ok = false;
+              break;
+            }
+            const int h = g * G + gh, q0 = p.col_q[c0 + c] * B_TILE_Q + t * 128;
+            const uint32_t dst = sb + L::ST_OFF + st * 2 * BL::TILE;
+            mbar_arrive_expect_tx(bar(L::B_SF + st), 2 * BL::TILE);
+            for (int hh = 0; hh < BL::NHALF; ++hh) {
+              tma_load_2d(dst + hh * BL::HALF, &tm_q, bar(L::B_SF + st), h * D + hh * 64, q0);
+              tma_load_2d(dst + BL::TILE + hh * BL::HALF, &tm_do, bar(L::B_SF + st), h * D + hh * 64, q0);
+            }
+            ++s;
+          }
+      if (*abort) {
+        wait_drain(bar(L::B_KV), 0, 20000000ull);
+        for (uint32_t i = (s > 2 ? s - 2 : 0); i < s; ++i) wait_drain(bar(L::B_SF + (i & 1)), (i >> 1) & 1, 20000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0 && nc > 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 1);
+      const uint32_t ks = sb + L::K_OFF, vs = sb + L::V_OFF;
+      bool ok = mbar_wait_bounded(bar(L::B_KV), 0, abort, lim);
+      uint32_t s = 0;
+      for (int c = 0; ok && c < nc; ++c)
+        for (int gh = 0; ok && gh < G; ++gh)
+          for (int t = 0; ok && t < 2; ++t) {
+            if (!half_ok(c, t)) continue;
+            const int st = s & 1;
+            const uint32_t qs = sb + L::ST_OFF + st * 2 * BL::TILE, dos = qs + BL::TILE;
+            if (!mbar_wait_bounded(bar(L::B_SF + st), (s >> 1) & 1, abort, lim)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
+              mma_ss(tmem, smem_desc_sw128(ks + off, 16, 1024), smem_desc_sw128(qs + off, 16, 1024),
+                     IDESC_QK, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
+              mma_ss(tmem + 128, smem_desc_sw128(vs + off, 16, 1024),
+                     smem_desc_sw128(dos + off, 16, 1024), IDESC_QK, kk > 0);
+            }
+            mma_commit(bar(L::B_ST));
+            if (!mbar_wait_bounded(bar(L::B_P), s & 1, abort, lim)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              mma_ts(tmem + 256, tmem + kk * 8, smem_desc_sw128(dos + kk * 16 * 128, BL::HALF, 1024),
+                     IDESC_PV, (s > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(tmem + 384, tmem + 128 + kk * 8, smem_desc_sw128(qs + kk * 16 * 128, BL::HALF, 1024),
+                     IDESC_PV, (s > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(bar(L::B_SE + st));
+            ++s;
+          }
+      if (ok) mma_commit(bar(L::B_O));
+      mma_commit(bar(L::B_DR));
+      wait_drain(bar(L::B_DR), 0, 20000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ element-wise (thread = key row)
+    const int r = warp * 32 + lane;
+    const int key = kt * 128 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t s = 0;
+    bool ok = true, any = false;
+    for (int c = 0; ok && c < nc; ++c) {
+      const int qt = p.col_q[c0 + c], e = p.col_e[c0 + c];
+      const int kd = p.kind[e], r0 = p.ref_ptr[e], r1 = p.ref_ptr[e + 1];
+      for (int gh = 0; ok && gh < G; ++gh)
+        for (int t = 0; ok && t < 2; ++t) {
+          if (!half_ok(c, t)) continue;
+          const int h = g * G + gh, q0 = qt * B_TILE_Q + t * 128;
+          float *vl = vec + (s & 1) * 256, *vd = vl + 128;
+          {
+            const int i = q0 + r;
+            const float lv = i < p.sq ? p.lse[static_cast<size_t>(h) * p.sq + i] : -INFINITY;
+            vl[r] = lv == -INFINITY ? INFINITY : lv * LOG2E;
+            vd[r] = i < p.sq ? p.delta[static_cast<size_t>(h) * p.sq + i] : 0.f;
+          }
+          // every element-wise thread has written its row's statistics
+          // (bounded wait: an abort elsewhere ends it)
+          mbar_arrive(bar(L::B_VEC));
+          if (!wait_all(bar(L::B_VEC), s & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
+          uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+          if (kd == ATTN_TILE_MASKED) {
+            w[0] = w[1] = w[2] = w[3] = 0u;
+            for (int q = r0; q < r1; ++q) add_col_mask(p.slices[p.ref_idx[q]], key, q0, w);
+          }
+          if (!wait_all(bar(L::B_ST), s & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          p_ds_step(tmem + lane_off, tmem + lane_off + 128, 0, 128, w, sl2,
+                    [&](int col) { return vl[col]; }, [&](int col) { return vd[col]; });
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(L::B_P));
+          any = true;
+          ++s;
+        }
+    }
+    // ---------------------------------------------------------- epilogue
+    bool have = ok && any;
+    if (have) {
+      have = wait_all(bar(L::B_O), 0, abort, lim);
+      tc_fence_after();
+    }
+    if (ok) {
+      // tensor-memory loads stay warp-uniform; only the stores depend on the row
+      const size_t off = (static_cast<size_t>(key) * p.hk + g) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t rv[32], rk[32];
+        if (have) {
+          tmem_ld32_wait(tmem + lane_off + 256 + cc * 32, rv);
+          tmem_ld32_wait(tmem + lane_off + 384 + cc * 32, rk);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) rv[k] = rk[k] = 0u;
+        }
+        if (key < p.sk) {
+          store_rows<D>(p.dv, p.grad_f32, off + cc * 32, rv, 1.f);
+          store_rows<D>(p.dk, p.grad_f32, off + cc * 32, rk, p.scale);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && *abort) atomicExch(&g_bwd_status, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
+}
+
+// ------------------------------------------------------------------ dQ per query tile
+// Work item: (query tile, head) as in the forward; the two 128-row halves in
+// turn.  Tensor memory: S [0,128)  dP [128,256)  dQ [256,256+D); dS (bf16)
+// overwrites the first 64 columns of S.
+template <int D, int NS>
+struct QLayout {
+  using B = BLayout<D>;
+  static constexpr int Q_OFF = 0, DO_OFF = B::TILE, KV_OFF = 2 * B::TILE;
+  static constexpr int BAR_OFF = KV_OFF + NS * B::TILE;
+  static constexpr int B_Q = 0, B_QE = 1, B_FULL = 2, B_EMPTY = 2 + NS, B_S = 2 + 2 * NS,
+                       B_P = B_S + 1, B_O = B_P + 1, B_DR = B_O + 1, NBAR = B_DR + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int ALLOC = MISC_OFF + 16 + 1024;
+};
+
+template <int D, int NS>
+__global__ void __launch_bounds__(B_THREADS, 1)
+    bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                 const BwdParams p) {
+  using L = QLayout<D, NS>;
+  using BL = BLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + L::BAR_OFF + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
+  volatile int *abort = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t lim = p.wait_ns;
+
+  const int qt = p.sched[blockIdx.x / p.hq];
+  const int h = blockIdx.x % p.hq;
+  const int g = h / (p.hq / p.hk);
+  const int e0 = p.row_ptr[qt], n = p.row_ptr[qt + 1] - e0;
+  const int halves = (qt * B_TILE_Q + 128 < p.sq) ? 2 : 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::B_Q), 1);
+    mbar_init(bar(L::B_QE), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar(L::B_FULL + s), 1);
+      mbar_init(bar(L::B_EMPTY + s), 1);
+    }
+    mbar_init(bar(L::B_S), 1);
+    mbar_init(bar(L::B_P), 128);
+    mbar_init(bar(L::B_O), 1);
+    mbar_init(bar(L::B_DR), 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    if (lane == 0 && n > 0) {
+      uint32_t ld = 0;
+      bool ok = true;
+      for (int t = 0; ok && t < halves; ++t) {
+        if (t > 0 && !mbar_wait_bounded(bar(L::B_QE), (t - 1) & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        const int q0 = qt * B_TILE_Q + t * 128;
+        mbar_arrive_expect_tx(bar(L::B_Q), 2 * BL::TILE);
+        for (int hh = 0; hh < BL::NHALF; ++hh) {
+          tma_load_2d(sb + L::Q_OFF + hh * BL::HALF, &tm_q, bar(L::B_Q), h * D + hh * 64, q0);
+          tma_load_2d(sb + L::DO_OFF + hh * BL::HALF, &tm_do, bar(L::B_Q), h * D + hh * 64, q0);
+        }
+        for (int i = 0; ok && i < 2 * n; ++i, ++ld) {
+          const int slot = ld % NS;
+          const uint32_t use = ld / NS;
+          if (use > 0 && !mbar_wait_bounded(bar(L::B_EMPTY + slot), (use - 1) & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
+          const int kt = p.col_idx[e0 + (i >> 1)];
+          mbar_arrive_expect_tx(bar(L::B_FULL + slot), BL::TILE);
+          for (int hh = 0; hh < BL::NHALF; ++hh)
+            tma_load_2d(sb + L::KV_OFF + slot * BL::TILE + hh * BL::HALF, (i & 1) ? &tm_v : &tm_k,
+                        bar(L::B_FULL + slot), g * D + hh * 64, kt * 128);
+        }
+      }
+      if (*abort) {
+        wait_drain(bar(L::B_Q), 0, 20000000ull);
+        const uint32_t from = ld > static_cast<uint32_t>(NS) ? ld - NS : 0;
+        for (uint32_t i = from; i < ld; ++i) wait_drain(bar(L::B_FULL + i % NS), (i / NS) & 1, 20000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 1);
+      const uint32_t qs = sb + L::Q_OFF, dos = sb + L::DO_OFF;
+      uint32_t ld = 0, s = 0;
+      bool ok = true;
+      for (int t = 0; ok && t < halves; ++t) {
+        if (!mbar_wait_bounded(bar(L::B_Q), t & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        for (int j = 0; j < n; ++j, ld += 2, ++s) {
+          const uint32_t kpos = ld, vpos = ld + 1;
+          const uint32_t kb = sb + L::KV_OFF + (kpos % NS) * BL::TILE;
+          const uint32_t vb = sb + L::KV_OFF + (vpos % NS) * BL::TILE;
+          if (!mbar_wait_bounded(bar(L::B_FULL + kpos % NS), (kpos / NS) & 1, abort, lim) ||
+              !mbar_wait_bounded(bar(L::B_FULL + vpos % NS), (vpos / NS) & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
+            mma_ss(tmem, smem_desc_sw128(qs + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                   IDESC_QK, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
+            mma_ss(tmem + 128, smem_desc_sw128(dos + off, 16, 1024), smem_desc_sw128(vb + off, 16, 1024),
+                   IDESC_QK, kk > 0);
+          }
+          mma_commit(bar(L::B_S));
+          mma_commit(bar(L::B_EMPTY + vpos % NS));
+          if (j == n - 1) mma_commit(bar(L::B_QE));
+          if (!mbar_wait_bounded(bar(L::B_P), s & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + 256, tmem + kk * 8, smem_desc_sw128(kb + kk * 16 * 128, BL::HALF, 1024),
+                   IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(L::B_EMPTY + kpos % NS));
+        }
+        if (ok) mma_commit(bar(L::B_O));
+      }
+      mma_commit(bar(L::B_DR));
+      wait_drain(bar(L::B_DR), 0, 20000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ element-wise (thread = query row)
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t s = 0;
+    bool ok = true;
+    for (int t = 0; ok && t < halves; ++t) {
+      const int row = qt * B_TILE_Q + t * 128 + warp * 32 + lane;
+      const bool live = row < p.sq;
+      const float lv = live ? p.lse[static_cast<size_t>(h) * p.sq + row] : -INFINITY;
+      const float lse2 = lv == -INFINITY ? INFINITY : lv * LOG2E;
+      const float dlt = live ? p.delta[static_cast<size_t>(h) * p.sq + row] : 0.f;
+      for (int j = 0; j < n; ++j, ++s) {
+        const int e = e0 + j;
+        const int kt = p.col_idx[e];
+        uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        if (p.kind[e] == ATTN_TILE_MASKED) {
+          w[0] = w[1] = w[2] = w[3] = 0u;
+          for (int q = p.ref_ptr[e]; q < p.ref_ptr[e + 1]; ++q)
+            add_mask(p.slices[p.ref_idx[q]], row, kt * 128, w);
+        }
+        if (!wait_all(bar(L::B_S), s & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        p_ds_step(tmem + lane_off, tmem + lane_off + 128, -1, 0, w, sl2,
+                  [&](int) { return lse2; }, [&](int) { return dlt; });
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::B_P));
+      }
+      if (!ok) break;
+      bool have = n > 0;
+      if (have) {
+        if (!wait_all(bar(L::B_O), t & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        if (have) {
+          tmem_ld32_wait(tmem + lane_off + 256 + cc * 32, r);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = 0u;
+        }
+        if (live) store_rows<D>(p.dq, p.grad_f32, (static_cast<size_t>(row) * p.hq + h) * D + cc * 32, r, p.scale);
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && *abort) atomicExch(&g_bwd_status, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
+}
+
+// ------------------------------------------------------------------ host side
+
+template <typename KernelT>
+static int set_smem(KernelT k, int bytes) {
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}
+
+template <int D>
+static int launch_bwd_main(const CUtensorMap *m, const BwdParams &p, cudaStream_t s) {
+  constexpr int NS = D == 128 ? 4 : 8;
+  int rc;
+  if ((rc = set_smem(bwd_kv_kernel<D>, KVLayout<D>::ALLOC)) != ATTN_OK) return rc;
+  if ((rc = set_smem(bwd_q_kernel<D, NS>, QLayout<D, NS>::ALLOC)) != ATTN_OK) return rc;
+  if (p.n_ktiles > 0)
+    bwd_kv_kernel<D><<<p.n_ktiles * p.hk, B_THREADS, KVLayout<D>::ALLOC, s>>>(m[0], m[1], m[2], m[3], p);
+  if (p.n_qtiles > 0)
+    bwd_q_kernel<D, NS><<<p.n_qtiles * p.hq, B_THREADS, QLayout<D, NS>::ALLOC, s>>>(m[0], m[1], m[2], m[3], p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t bwd_workspace_bytes(int sq, int hq, int n_ktiles, int64_t cap_entries) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  return up(sizeof(float) * static_cast<size_t>(sq) * hq) + up(sizeof(int32_t) * n_ktiles) +
+         up(sizeof(int32_t) * (n_ktiles + 1)) + up(sizeof(int32_t) * n_ktiles) +
+         2 * up(sizeof(int32_t) * static_cast<size_t>(cap_entries > 0 ? cap_entries : 1));
+}
+
+int bwd_launch(const void *q, const void *k, const void *v, const void *out, int out_dtype,
+               const void *dout, const float *lse, int sq, int sk, int hq, int hk, int d, float scale,
+               const attn_tiles_t *tiles, void *dq, void *dk, void *dv, int grad_dtype, void *d_ws,
+               cudaStream_t stream) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  uint8_t *ws = static_cast<uint8_t *>(d_ws);
+  const int nk = tiles->n_ktiles;
+  float *delta = reinterpret_cast<float *>(ws);
+  ws += up(sizeof(float) * static_cast<size_t>(sq) * hq);
+  int32_t *colcnt = reinterpret_cast<int32_t *>(ws);
+  ws += up(sizeof(int32_t) * nk);
+  int32_t *col_ptr = reinterpret_cast<int32_t *>(ws);
+  ws += up(sizeof(int32_t) * (nk + 1));
+  int32_t *col_sched = reinterpret_cast<int32_t *>(ws);
+  ws += up(sizeof(int32_t) * nk);
+  const size_t cap = up(sizeof(int32_t) * static_cast<size_t>(tiles->cap_entries > 0 ? tiles->cap_entries : 1));
+  int32_t *col_q = reinterpret_cast<int32_t *>(ws);
+  int32_t *col_e = reinterpret_cast<int32_t *>(ws + cap);
+
+  BwdParams p;
+  p.row_ptr = tiles->row_ptr;
+  p.col_idx = tiles->col_idx;
+  p.ref_ptr = tiles->ref_ptr;
+  p.ref_idx = tiles->ref_idx;
+  p.sched = tiles->sched;
+  p.kind = tiles->kind;
+  p.slices = tiles->slices;
+  p.col_ptr = col_ptr;
+  p.col_q = col_q;
+  p.col_e = col_e;
+  p.col_sched = col_sched;
+  p.lse = lse;
+  p.delta = delta;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.sq = sq;
+  p.sk = sk;
+  p.hq = hq;
+  p.hk = hk;
+  p.n_qtiles = tiles->n_qtiles;
+  p.n_ktiles = nk;
+  p.grad_f32 = grad_dtype == ATTN_DTYPE_F32;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.wait_ns = wait_limit_ns();
+
+  const long long warps = static_cast<long long>(sq) * hq;
+  const unsigned dgrid = static_cast<unsigned>((warps * 32 + 255) / 256);
+  const uint16_t *dob = static_cast<const uint16_t *>(dout);
+  if (d == 128) {
+    if (out_dtype == ATTN_DTYPE_F32) bwd_delta_kernel<128, true><<<dgrid, 256, 0, stream>>>(out, dob, delta, sq, hq);
+    else bwd_delta_kernel<128, false><<<dgrid, 256, 0, stream>>>(out, dob, delta, sq, hq);
+  } else {
+    if (out_dtype == ATTN_DTYPE_F32) bwd_delta_kernel<64, true><<<dgrid, 256, 0, stream>>>(out, dob, delta, sq, hq);
+    else bwd_delta_kernel<64, false><<<dgrid, 256, 0, stream>>>(out, dob, delta, sq, hq);
+  }
+  if (nk > 0) {
+    csc_count_kernel<<<nk, 256, 0, stream>>>(p, colcnt);
+    csc_fill_kernel<<<nk, 256, 0, stream>>>(p, colcnt, col_ptr, col_q, col_e, col_sched);
+  }
+  CUtensorMap m[4];
+  int rc;
+  if ((rc = make_tma_2d(&m[0], q, static_cast<uint64_t>(hq) * d, sq)) != ATTN_OK) return rc;
+  if ((rc = make_tma_2d(&m[1], k, static_cast<uint64_t>(hk) * d, sk)) != ATTN_OK) return rc;
+  if ((rc = make_tma_2d(&m[2], v, static_cast<uint64_t>(hk) * d, sk)) != ATTN_OK) return rc;
+  if ((rc = make_tma_2d(&m[3], dout, static_cast<uint64_t>(hq) * d, sq)) != ATTN_OK) return rc;
+  if (d == 128) return launch_bwd_main<128>(m, p, stream);
+  return launch_bwd_main<64>(m, p, stream);
+}
+
+int bwd_status_take(unsigned int *status) {
+  unsigned int zero = 0;
+  if (cudaMemcpyFromSymbol(status, g_bwd_status, sizeof(unsigned int)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (*status && cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(unsigned int)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+}  // namespace attn

@@ -35,8 +35,6 @@
 // softmax of tile t sees S_t(j) its previous PV_t(j-1) has completed too,
 // and the next item's first QK may be issued while the softmax warps are
 // still storing the previous item's O (its first PV waits for their P).
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -44,8 +42,8 @@
 #include <cstdint>
 #include <mutex>
 
+#include "attn_device.cuh"
 #include "attn_internal.h"
-#include "ptx.cuh"
 
 namespace attn {
 
@@ -105,62 +103,6 @@ struct Layout {
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;
 };
-
-__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int *abort,
-                                         uint64_t limit) {
-  bool ok = mbar_wait_bounded(bar, parity, abort, limit);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Waits for in-flight asynchronous work before tensor memory and shared
-// memory are released on the failure path; bounded independently of *abort.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t dl = globaltimer_ns() + limit_ns;
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() > dl) break;
-  }
-}
-
-__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
-  tmem_ld32(taddr, r);
-  tmem_wait_ld();
-#pragma unroll
-  for (int k = 0; k < 32; ++k) asm volatile("" : "+r"(r[k]));
-}
-
-__device__ __forceinline__ uint32_t bits_below(int x) {   // bits [0, x) set, 0 <= x <= 32
-  return x >= 32 ? 0xffffffffu : ((1u << x) - 1u);
-}
-
-// Valid key interval [lo, hi) of slice `s` for query row i (global indices);
-// empty (lo == hi) when row i is outside the slice.
-__device__ __forceinline__ void slice_interval(const attn_slice_t &s, int i, int &lo, int &hi) {
-  if (i < s.q_start || i >= s.q_end) {
-    lo = hi = 0;
-    return;
-  }
-  const int a = i - s.q_start, lq = s.q_end - s.q_start, lk = s.k_end - s.k_start;
-  int l = 0, h = lk;
-  if (s.type == 1 || s.type == 3) h = min(h, a + (lk - lq) + 1);
-  if (s.type == 2 || s.type == 3) l = max(l, a);
-  if (h < l) h = l;
-  lo = s.k_start + l;
-  hi = s.k_start + h;
-}
-
-// ORs the valid columns of slice `s` for row `row` inside key tile [c0, c0+128).
-__device__ __forceinline__ void add_mask(const attn_slice_t &s, int row, int c0, uint32_t (&w)[4]) {
-  int lo, hi;
-  slice_interval(s, row, lo, hi);
-  lo = min(max(lo - c0, 0), BN);
-  hi = min(max(hi - c0, 0), BN);
-  if (hi <= lo) return;
-#pragma unroll
-  for (int c = 0; c < BN / 32; ++c) {
-    const int a = min(max(lo - 32 * c, 0), 32), b = min(max(hi - 32 * c, 0), 32);
-    w[c] |= bits_below(b) & ~bits_below(a);
-  }
-}
 
 struct Item {
   int qt, h, g, e0, n;
@@ -616,35 +558,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // ------------------------------------------------------------------ host side
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 2-D bf16 map over a [rows, cols] row-major matrix, 64 x 128 boxes with
-// the 128-byte swizzle the MMA descriptors expect.
-static int make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows) {
-  auto enc = get_encode_fn();
-  if (!enc) return ATTN_ERR_CUDA;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 128};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
 static unsigned long long g_wait_ns = 4000000000ull;
 constexpr int kMaxDev = 64;
 static std::atomic<unsigned int> g_launch_seq{0};
@@ -665,19 +578,6 @@ static unsigned int *next_counter() {
     }
   }
   return base[dev] + (g_launch_seq.fetch_add(1) % SCHED_SLOTS);
-}
-
-static int sm_count() {
-  static int cached[kMaxDev] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return -1;
-  if (!cached[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      return -1;
-    cached[dev] = n;
-  }
-  return cached[dev];
 }
 
 template <int D, int NS>
@@ -702,9 +602,9 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
                cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   int rc;
-  if ((rc = make_map(&mq, q, static_cast<uint64_t>(hq) * d, sq)) != ATTN_OK) return rc;
-  if ((rc = make_map(&mk, k, static_cast<uint64_t>(hk) * d, sk)) != ATTN_OK) return rc;
-  if ((rc = make_map(&mv, v, static_cast<uint64_t>(hk) * d, sk)) != ATTN_OK) return rc;
+  if ((rc = make_tma_2d(&mq, q, static_cast<uint64_t>(hq) * d, sq)) != ATTN_OK) return rc;
+  if ((rc = make_tma_2d(&mk, k, static_cast<uint64_t>(hk) * d, sk)) != ATTN_OK) return rc;
+  if ((rc = make_tma_2d(&mv, v, static_cast<uint64_t>(hk) * d, sk)) != ATTN_OK) return rc;
   FwdParams p;
   p.row_ptr = tiles->row_ptr;
   p.col_idx = tiles->col_idx;
@@ -726,7 +626,7 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   if (items == 0) return ATTN_OK;
   if (items >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   p.n_items = static_cast<int>(items);
-  const int sms = sm_count();
+  const int sms = device_sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   const int grid = static_cast<int>(items < sms ? items : sms);
   p.counter = next_counter();
@@ -746,6 +646,8 @@ int fwd_status_take(unsigned int *status) {
 }
 
 void fwd_set_wait_ns(unsigned long long ns) { g_wait_ns = ns; }
+
+unsigned long long wait_limit_ns() { return g_wait_ns; }
 
 // One thread waits on a barrier that nothing will complete; the bounded wait
 // gives up after the configured limit and records a timeout.

@@ -216,8 +216,30 @@ int attn_merge(const void *const *h_o_parts, const float *const *h_lse_parts, in
                int part_dtype, int s_len, int h, int d, void *out, int out_dtype, float *lse,
                attn_stream_t stream);
 
+/* Backward pass of the masked attention forward: gradients of a loss L with
+ * respect to Q, K, V given dO = dL/dO, for the same tile metadata.  P is
+ * recomputed from the forward's lse:  D = rowsum(dO * O),  dP = dO V^T,
+ * dS = P * (dP - D),  dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K
+ * (heads of a GQA group summed into dK, dV).  The pages list the backward
+ * pass alongside the forward (MagiAttention page: forward and backward kernel
+ * benchmarks; FlashAttention-4 page: a rebuilt backward pipeline); the
+ * formulas are the chain rule through the softmax.
+ *   q, k, v, dout   bf16 [S_q,H,d], [S_k,H_k,d], [S_k,H_k,d], [S_q,H,d]
+ *   out, out_dtype  the forward output O (bf16 or f32) for D
+ *   lse             [H, S_q] f32 from the forward
+ *   dq, dk, dv      [S_q,H,d], [S_k,H_k,d], [S_k,H_k,d] of grad_dtype
+ *   d_ws            >= attn_bwd_workspace_bytes() bytes (D, transposed lists)
+ * No atomics: dK, dV are accumulated per key tile over its query tiles (a
+ * transposed copy of the lists built on the device), dQ per query tile.
+ * Errors: as attn_fwd, plus CAPACITY when ws_bytes is too small. */
+int attn_bwd_workspace_bytes(const attn_tiles_t *tiles, int hq, size_t *bytes);
+int attn_bwd(const void *q, const void *k, const void *v, const void *out, int out_dtype,
+             const void *dout, const float *lse, int sq, int sk, int hq, int hk, int d, float scale,
+             const attn_tiles_t *tiles, void *dq, void *dk, void *dv, int grad_dtype, void *d_ws,
+             size_t ws_bytes, attn_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device-side status of
- * the forward kernels on the current device: ATTN_OK, or ATTN_ERR_TIMEOUT when
+ * the forward and backward kernels on the current device: ATTN_OK, or ATTN_ERR_TIMEOUT when
  * a bounded wait ran out (the kernel then left its outputs incomplete). */
 int attn_last_device_error(attn_stream_t stream);
 
