@@ -31,6 +31,10 @@
 //   PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1)
 // so the tensor core works on one tile while the softmax warps of the other
 // tile run (FlashAttention-4 page: softmax overlapped with the MMAs).
+// The epilogue of a bf16 output stages each 128 x 64 half of O_t / l in
+// shared memory (the 128-byte swizzle of the output's tensor map) and leaves
+// it with one TMA store, which writes whole rows and clips the rows past
+// S_q; f32 partial outputs keep one thread per row.
 // tcgen05 operations of one thread complete in issue order, so when the
 // softmax of tile t sees S_t(j) its previous PV_t(j-1) has completed too,
 // and the next item's first QK may be issued while the softmax warps are
@@ -53,7 +57,7 @@ constexpr int BM = 128;           // rows per MMA tile
 constexpr int BN = 128;           // keys per KV tile
 constexpr float TAU = 8.0f;       // lazy-rescale threshold, log2 units
 constexpr int NTHREADS = 352;
-constexpr int RING = 32;          // metadata records in flight
+constexpr int RING = 16;          // metadata records in flight
 constexpr int IQ = 4;             // queued work-item ids
 constexpr int SCHED_SLOTS = 4096; // work counters, one per launch in flight
 
@@ -68,7 +72,7 @@ struct FwdParams {
   void *out;
   float *lse;
   int sq, sk, hq, hk, n_items;
-  int out_f32;
+  int out_f32;                    // f32 O by direct stores, else bf16 O by TMA stores
   float scale_log2;               // scale * log2(e)
   unsigned long long wait_ns;
   unsigned int *counter;          // this launch's work counter (zeroed before launch)
@@ -90,18 +94,22 @@ struct Layout {
   static constexpr int TILE = NHALF * HALF;          // 128 x D bf16
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TILE;
-  static constexpr int REC_OFF = KV_OFF + NS * TILE;
+  static constexpr int ST_OFF = KV_OFF + NS * TILE;   // bf16 O staging: one 128 x 64 half per tile
+  static constexpr int REC_OFF = ST_OFF + 2 * HALF;
   static constexpr int IQ_OFF = REC_OFF + RING * 64;
   static constexpr int BAR_OFF = IQ_OFF + IQ * 16;
   // q_full | q_empty | full[NS] | empty[NS] | s_full[2] | p_full[2] | o_full[2] | drain |
-  // rec_full[RING] | rec_empty[RING] | iq_full[IQ] | iq_empty[IQ]
+  // rec_full[RING] | rec_empty[RING] | iq_full[IQ] | iq_empty[IQ] | stage_full[2] |
+  // stage_free[2]
   static constexpr int B_Q = 0, B_QE = 1, B_FULL = 2, B_EMPTY = 2 + NS, B_S = 2 + 2 * NS,
                        B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2, B_RF = B_DRAIN + 1,
                        B_RE = B_RF + RING, B_IF = B_RE + RING, B_IE = B_IF + IQ,
-                       NBAR = B_IE + IQ;
+                       B_EF = B_IE + IQ, B_EE = B_EF + 2, NBAR = B_EE + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;
+  static_assert(ST_OFF % 1024 == 0, "swizzled staging alignment");
+  static_assert(ALLOC <= 232448, "shared memory per CTA");
 };
 
 struct Item {
@@ -121,7 +129,8 @@ __device__ __forceinline__ Item decode(const FwdParams &p, int item) {
 template <int D, int NS>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const FwdParams p) {
   using L = Layout<D, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -158,6 +167,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int u = 0; u < IQ; ++u) {
       mbar_init(bar(L::B_IF + u), 1);
       mbar_init(bar(L::B_IE + u), 10);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::B_EF + t), 128);
+      mbar_init(bar(L::B_EE + t), 1);
     }
     *abort = 0;
     fence_mbar_init();
@@ -237,7 +250,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);
-      auto issue_qk = [&](int t, int slot) {
+      auto issue_qk = [=](int t, int slot) {
         const uint32_t d_tmem = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -246,7 +259,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                  smem_desc_sw128(kv_smem + slot * L::TILE + off, 16, 1024), IDESC_QK, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int slot, bool first) {
+      auto issue_pv = [=](int t, int slot, bool first) {
         const uint32_t d_tmem = tmem + 256 + t * 128;
         const uint32_t a_tmem = tmem + t * 128;
 #pragma unroll
@@ -382,7 +395,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + 256 + t * 128;
     const float sl2 = p.scale_log2;
-    uint32_t step = 0, rpos = 0, nonempty = 0;
+    uint32_t step = 0, rpos = 0, nonempty = 0, ep = 0;
     bool ok = true;
     uint32_t qpos = 0;
     while (ok) {
@@ -511,34 +524,71 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        if (it.n > 0) {
-          tmem_ld32_wait(tO + c * 32, r);
-        } else {
+      if (!p.out_f32) {
+        // bf16 O through a 128 x 64 shared-memory half in the 128-byte
+        // swizzle of the output's tensor map (16-byte chunk c of row r at
+        // chunk c ^ (r & 7)), one TMA store per half; the store clips the
+        // rows past S_q
+        const uint32_t stg = sb + L::ST_OFF + t * L::HALF;
+        const int r = wl * 32 + lane;
+        const bool elected = wl == 0 && lane == 0;
+        const int y0 = it.qt * 256 + t * BM;
+        for (int hh = 0; hh < L::NHALF; ++hh) {
+          // the previous store out of this half has finished reading it
+          if (ep > 0 && !wait_all(bar(L::B_EE + t), (ep - 1) & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
 #pragma unroll
-          for (int k = 0; k < 32; ++k) r[k] = 0u;
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t x[32];
+            if (it.n > 0) {
+              tmem_ld32_wait(tO + hh * 64 + c2 * 32, x);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) x[k] = 0u;
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(x[8 * q4 + 0]) * inv, __uint_as_float(x[8 * q4 + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(x[8 * q4 + 2]) * inv, __uint_as_float(x[8 * q4 + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(x[8 * q4 + 4]) * inv, __uint_as_float(x[8 * q4 + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(x[8 * q4 + 6]) * inv, __uint_as_float(x[8 * q4 + 7]) * inv);
+              st_shared_v4(stg + r * 128 + (((c2 * 4 + q4) ^ (r & 7)) << 4), v);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(L::B_EF + t));
+          if (elected) {
+            if (mbar_wait_bounded(bar(L::B_EF + t), ep & 1, abort, lim) && y0 < p.sq) {
+              tma_store_2d(&tm_o, stg, it.h * D + hh * 64, y0);
+              bulk_commit_group();
+              bulk_wait_read_all();
+            }
+            mbar_arrive(bar(L::B_EE + t));
+          }
+          ++ep;
         }
-        if (!live) continue;
-        if (p.out_f32) {
+        if (!ok) break;
+      } else {
+        // f32 O (KV-split partials): one thread per row, 16-byte stores
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          if (it.n > 0) {
+            tmem_ld32_wait(tO + c * 32, r);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) r[k] = 0u;
+          }
+          if (!live) continue;
           float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + obase + c * 32);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
                                  __uint_as_float(r[4 * k + 2]) * inv,
                                  __uint_as_float(r[4 * k + 3]) * inv);
-        } else {
-          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + obase + c * 32);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv);
-            dst[k] = v;
-          }
         }
       }
       if (live)
@@ -547,6 +597,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // tensor-memory reads of O finish before the next item's first PV
       tc_fence_before();
     }
+    // the output stores have completed before the CTA retires
+    if (wl == 0 && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -582,7 +634,7 @@ static unsigned int *next_counter() {
 
 template <int D, int NS>
 static int launch_fwd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                      const FwdParams &p, int grid, cudaStream_t s) {
+                      const CUtensorMap &mo, const FwdParams &p, int grid, cudaStream_t s) {
   using L = Layout<D, NS>;
   static bool configured[kMaxDev] = {};
   int dev = 0;
@@ -593,14 +645,14 @@ static int launch_fwd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtens
       return ATTN_ERR_CUDA;
     configured[dev] = true;
   }
-  fwd_kernel<D, NS><<<grid, NTHREADS, L::ALLOC, s>>>(mq, mk, mv, p);
+  fwd_kernel<D, NS><<<grid, NTHREADS, L::ALLOC, s>>>(mq, mk, mv, mo, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int hq, int hk, int d,
                float scale, const attn_tiles_t *tiles, void *out, int out_dtype, float *lse,
                cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   int rc;
   if ((rc = make_tma_2d(&mq, q, static_cast<uint64_t>(hq) * d, sq)) != ATTN_OK) return rc;
   if ((rc = make_tma_2d(&mk, k, static_cast<uint64_t>(hk) * d, sk)) != ATTN_OK) return rc;
@@ -620,6 +672,13 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   p.hq = hq;
   p.hk = hk;
   p.out_f32 = out_dtype == ATTN_DTYPE_F32;
+  // bf16 O is stored by TMA through the same 64 x 128 box format as Q; the
+  // f32 path (partials) keeps one thread per row and needs no map
+  if (!p.out_f32) {
+    if ((rc = make_tma_2d(&mo, out, static_cast<uint64_t>(hq) * d, sq)) != ATTN_OK) return rc;
+  } else {
+    mo = mq;
+  }
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_ns = g_wait_ns;
   const long long items = static_cast<long long>(tiles->n_qtiles) * hq;
@@ -632,8 +691,8 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   p.counter = next_counter();
   if (!p.counter || cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  if (d == 128) return launch_fwd<128, 4>(mq, mk, mv, p, grid, stream);
-  return launch_fwd<64, 8>(mq, mk, mv, p, grid, stream);
+  if (d == 128) return launch_fwd<128, 4>(mq, mk, mv, mo, p, grid, stream);
+  return launch_fwd<64, 8>(mq, mk, mv, mo, p, grid, stream);
 }
 
 int fwd_status_take(unsigned int *status) {
