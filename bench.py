@@ -51,6 +51,9 @@ def parse():
                     help="fwd: the forward hot path (default); bwd: attn_bwd alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--exp2-poly", type=int, default=0, choices=[0, 4, 8],
+                    help="forward exponentials: 0 all on the special-function unit (default); "
+                         "4 / 8 every 4th / 8th pair of a FULL tile on the FMA-pipe polynomial")
     return ap.parse_args()
 
 
@@ -282,6 +285,7 @@ def gpu_arm(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pkg.load()
+    pkg.attn_set_exp2_poly(args.exp2_poly)
     w = W.ALL[args.workload]()
     sl = slices_of(w)
     q, k, v = W.draw_qkv(w.S, w.H, w.Hk, w.d, w.seed)
@@ -406,7 +410,8 @@ def gpu_arm(args, ws, rank, local):
     fwd_s = fwd_mean / 1e3
     achieved = flops / fwd_s / 1e12
     src = os.path.join(ROOT, "block_sparse_attention_slice_gb300", "csrc", "fwd_tcgen05.cu")
-    traffic = profile_traffic("attn_fwd", w.name, src)
+    # the committed counters were taken with the default exponential path
+    traffic = profile_traffic("attn_fwd", w.name, src) if args.exp2_poly == 0 else None
     roof = {"kernel": "attn_fwd", "bound": "tensor", "achieved": achieved,
             "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
             "traffic": traffic, "peak_source": f"bf16_tflops (burst) of {pk_src}",
@@ -436,6 +441,7 @@ def gpu_arm(args, ws, rank, local):
                 "config": {"workload": w.name, "S": w.S, "H": w.H, "Hk": w.Hk, "d": w.d,
                            "valid_pairs_per_head": pairs_per_head, "tiles_nnz": nnz,
                            "kv_split_parts": len(split), "l2": "flushed between timed steps",
+                           "exp2_poly": args.exp2_poly,
                            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
                 "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16_tflops"],
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,

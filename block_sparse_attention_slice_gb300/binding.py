@@ -27,7 +27,8 @@ EXPORTS = ["attn_tiles_workspace_bytes", "attn_build_tiles", "attn_build_tiles_n
            "attn_tiles_totals",
            "attn_slices_from_block_grid", "attn_fwd", "attn_merge", "attn_bwd_workspace_bytes",
            "attn_bwd", "attn_last_device_error",
-           "attn_set_wait_limit_ns", "attn_selftest_wait_timeout", "attn_strerror"]
+           "attn_set_wait_limit_ns", "attn_set_exp2_poly", "attn_selftest_wait_timeout",
+           "attn_strerror"]
 
 
 class AttnSlice(ctypes.Structure):
@@ -81,6 +82,7 @@ def load(path: Optional[str] = None):
                              ctypes.POINTER(AttnTiles), vp, vp, vp, i32, vp, sz, vp]
     lib.attn_last_device_error.argtypes = [vp]
     lib.attn_set_wait_limit_ns.argtypes = [i64]
+    lib.attn_set_exp2_poly.argtypes = [i32]
     lib.attn_selftest_wait_timeout.argtypes = [vp]
     lib.attn_strerror.argtypes = [i32]
     lib.attn_strerror.restype = ctypes.c_char_p
@@ -305,6 +307,13 @@ def attn_last_device_error(stream=None) -> int:
 
 def attn_set_wait_limit_ns(ns: int):
     _check(load().attn_set_wait_limit_ns(int(ns)), "attn_set_wait_limit_ns")
+
+
+def attn_set_exp2_poly(period: int):
+    """0: all exponentials on the special-function unit (default); 4 or 8:
+    every 4th / 8th pair of a FULL tile's exponentials on the FMA-pipe
+    polynomial.  Applies to later attn_fwd calls of this process."""
+    _check(load().attn_set_exp2_poly(int(period)), "attn_set_exp2_poly")
 
 
 def attn_selftest_wait_timeout(stream=None):

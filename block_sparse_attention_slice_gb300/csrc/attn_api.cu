@@ -338,6 +338,12 @@ int attn_set_wait_limit_ns(int64_t ns) {
   return ATTN_OK;
 }
 
+int attn_set_exp2_poly(int period) {
+  if (period != 0 && period != 4 && period != 8) return ATTN_ERR_INVALID_ARG;
+  attn::fwd_set_exp2_poly(period);
+  return ATTN_OK;
+}
+
 int attn_selftest_wait_timeout(attn_stream_t stream) {
   return attn::selftest_timeout_launch(reinterpret_cast<cudaStream_t>(stream));
 }

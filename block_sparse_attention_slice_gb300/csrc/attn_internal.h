@@ -47,6 +47,7 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
                cudaStream_t stream);
 int fwd_status_take(unsigned int *status);
 void fwd_set_wait_ns(unsigned long long ns);
+void fwd_set_exp2_poly(int period);
 unsigned long long wait_limit_ns();
 int selftest_timeout_launch(cudaStream_t s);
 

@@ -45,6 +45,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "attn_device.cuh"
 #include "attn_internal.h"
@@ -126,12 +127,16 @@ __device__ __forceinline__ Item decode(const FwdParams &p, int item) {
   return it;
 }
 
-template <int D, int NS>
+// POLY = 0: every exponential on the special-function unit; POLY = k > 0:
+// on FULL tiles, every k-th pair of a row's exponentials on the FMA-pipe
+// polynomial (exp2_poly2), the rest on the special-function unit.
+template <int D, int NS, int POLY>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const FwdParams p) {
   using L = Layout<D, NS>;
+  static_assert(POLY == 0 || (POLY > 0 && 16 % POLY == 0), "polynomial period");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -480,19 +485,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // two-wide partial sums
         const uint64_t sc2 = f2_make(sl2, sl2), nb2 = f2_make(-mb, -mb);
         uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
+        // USE_POLY: FULL tile with the polynomial enabled (all arguments
+        // finite); MASKED tiles keep the special-function unit, which maps
+        // a masked -inf to exactly 0
+        auto exps = [&](auto use_poly) {
+          constexpr bool USE_POLY = decltype(use_poly)::value;
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t pk[16];
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            float a0, a1;
-            f2_split(f2_fma(f2_make(s[c * 32 + 2 * k], s[c * 32 + 2 * k + 1]), sc2, nb2), a0, a1);
-            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-            l2[k & 3] = f2_add(l2[k & 3], f2_make(p0, p1));
-            pk[k] = pack_bf16x2(p0, p1);
+            for (int k = 0; k < 16; ++k) {
+              const uint64_t a2 = f2_fma(f2_make(s[c * 32 + 2 * k], s[c * 32 + 2 * k + 1]), sc2, nb2);
+              float p0, p1;
+              if (USE_POLY && (k % (POLY > 0 ? POLY : 1)) == (POLY > 0 ? POLY : 1) - 1) {
+                f2_split(exp2_poly2(a2), p0, p1);
+              } else {
+                float a0, a1;
+                f2_split(a2, a0, a1);
+                p0 = ex2_approx(a0);
+                p1 = ex2_approx(a1);
+              }
+              l2[k & 3] = f2_add(l2[k & 3], f2_make(p0, p1));
+              pk[k] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + c * 16, pk);
           }
-          tmem_st16(tS + c * 16, pk);
-        }
+        };
+        if (POLY > 0 && kd == ATTN_TILE_FULL)
+          exps(std::true_type{});
+        else
+          exps(std::false_type{});
         {
           float x0, x1;
           f2_split(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])), x0, x1);
@@ -611,6 +633,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // ------------------------------------------------------------------ host side
 
 static unsigned long long g_wait_ns = 4000000000ull;
+static int g_exp2_poly = 0;   // 0, 4 or 8: see fwd_kernel's POLY
 constexpr int kMaxDev = 64;
 static std::atomic<unsigned int> g_launch_seq{0};
 
@@ -632,7 +655,7 @@ static unsigned int *next_counter() {
   return base[dev] + (g_launch_seq.fetch_add(1) % SCHED_SLOTS);
 }
 
-template <int D, int NS>
+template <int D, int NS, int POLY>
 static int launch_fwd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                       const CUtensorMap &mo, const FwdParams &p, int grid, cudaStream_t s) {
   using L = Layout<D, NS>;
@@ -640,12 +663,12 @@ static int launch_fwd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtens
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
   if (!configured[dev]) {
-    if (cudaFuncSetAttribute(fwd_kernel<D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(fwd_kernel<D, NS, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::ALLOC) != cudaSuccess)
       return ATTN_ERR_CUDA;
     configured[dev] = true;
   }
-  fwd_kernel<D, NS><<<grid, NTHREADS, L::ALLOC, s>>>(mq, mk, mv, mo, p);
+  fwd_kernel<D, NS, POLY><<<grid, NTHREADS, L::ALLOC, s>>>(mq, mk, mv, mo, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -691,8 +714,15 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   p.counter = next_counter();
   if (!p.counter || cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  if (d == 128) return launch_fwd<128, 4>(mq, mk, mv, mo, p, grid, stream);
-  return launch_fwd<64, 8>(mq, mk, mv, mo, p, grid, stream);
+  const int poly = g_exp2_poly;
+  if (d == 128) {
+    if (poly == 4) return launch_fwd<128, 4, 4>(mq, mk, mv, mo, p, grid, stream);
+    if (poly == 8) return launch_fwd<128, 4, 8>(mq, mk, mv, mo, p, grid, stream);
+    return launch_fwd<128, 4, 0>(mq, mk, mv, mo, p, grid, stream);
+  }
+  if (poly == 4) return launch_fwd<64, 8, 4>(mq, mk, mv, mo, p, grid, stream);
+  if (poly == 8) return launch_fwd<64, 8, 8>(mq, mk, mv, mo, p, grid, stream);
+  return launch_fwd<64, 8, 0>(mq, mk, mv, mo, p, grid, stream);
 }
 
 int fwd_status_take(unsigned int *status) {
@@ -705,6 +735,8 @@ int fwd_status_take(unsigned int *status) {
 }
 
 void fwd_set_wait_ns(unsigned long long ns) { g_wait_ns = ns; }
+
+void fwd_set_exp2_poly(int period) { g_exp2_poly = period; }
 
 unsigned long long wait_limit_ns() { return g_wait_ns; }
 

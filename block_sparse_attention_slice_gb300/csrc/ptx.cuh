@@ -266,6 +266,49 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return d;
 }
 
+__device__ __forceinline__ uint64_t f2_make_u(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split_u(uint64_t v, uint32_t &lo, uint32_t &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+
+// 2^a for a pair of finite f32 arguments on the FMA pipe instead of the
+// special-function unit (FlashAttention-4 page, first technique: software
+// exponentials by polynomial approximation on the FMA units, mixed with the
+// hardware ones).  Range reduction 2^a = 2^n 2^f, n = round(a) by adding
+// 1.5 * 2^23 (the sum's low mantissa bits hold n), f = a - n in [-1/2, 1/2];
+// 2^f by a cubic in Horner form whose coefficients come from
+// exp2_poly_fit.py (least squares on Chebyshev nodes, relative weights,
+// c0 = 1 so 2^0 is exact; worst relative error 1.2e-4 in f32, below the
+// bf16 rounding of P); the integer n is added to the exponent field.  a is
+// clamped at -125 so the result stays a positive normal number (its
+// contribution next to a row sum of at least 1 is nil); -inf (a masked
+// score) is not a valid input.
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t a2) {
+  constexpr float kRound = 12582912.f;   // 1.5 * 2^23
+  constexpr float c3 = 0.05459282547235489f, c2 = 0.24221783876419067f,
+                  c1 = 0.6933686137199402f;
+  float a0, a1;
+  f2_split(a2, a0, a1);
+  const uint64_t x = f2_make(fmaxf(a0, -125.f), fmaxf(a1, -125.f));
+  const uint64_t t = f2_add(x, f2_make(kRound, kRound));
+  const uint64_t n = f2_add(t, f2_make(-kRound, -kRound));
+  const uint64_t f = f2_fma(n, f2_make(-1.f, -1.f), x);
+  uint64_t q = f2_fma(f2_make(c3, c3), f, f2_make(c2, c2));
+  q = f2_fma(q, f, f2_make(c1, c1));
+  q = f2_fma(q, f, f2_make(1.f, 1.f));
+  uint32_t t0, t1, q0, q1, r0, r1;
+  f2_split_u(t, t0, t1);
+  f2_split_u(q, q0, q1);
+  // (t_bits << 23) keeps only n << 23: the bits of 1.5 * 2^23 shift out
+  asm("mad.lo.u32 %0, %1, 8388608, %2;" : "=r"(r0) : "r"(t0), "r"(q0));
+  asm("mad.lo.u32 %0, %1, 8388608, %2;" : "=r"(r1) : "r"(t1), "r"(q1));
+  return f2_make_u(r0, r1);
+}
+
 // Packs two floats to bf16x2 (round to nearest even): `lo` in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -248,6 +248,21 @@ int attn_last_device_error(attn_stream_t stream);
  * with a short limit. */
 int attn_set_wait_limit_ns(int64_t ns);
 
+/* Selects where the exponentials of later attn_fwd launches (this process)
+ * run.  FlashAttention-4 page, first technique: part of the exponentials on
+ * the FMA units through a polynomial approximation, the rest on the
+ * special-function unit (MUFU), which that page notes runs twice as fast on
+ * GB300 as on B200.
+ *   period 0   every exponential on the special-function unit (default)
+ *   period 4/8 on FULL tiles, every 4th / 8th pair of exponentials of a row
+ *              through a cubic for 2^f after range reduction (worst relative
+ *              error 1.2e-4, below the bf16 rounding of P); MASKED tiles
+ *              always use the special-function unit
+ * Any other period: ATTN_ERR_INVALID_ARG.  Results stay within the forward's
+ * tolerances either way; the mode only trades special-function work for
+ * FMA-pipe instructions. */
+int attn_set_exp2_poly(int period);
+
 /* Failure-path self test: launches one CTA that waits, with the current wait
  * bound, on a barrier nothing will ever complete; the wait gives up, records
  * ATTN_ERR_TIMEOUT in the device status and the kernel returns normally.  Read
