@@ -38,6 +38,7 @@ import numpy as np
 METRIC = "masked attn fwd TFLOPS (valid-pair FLOPs) and % of GB300 BF16 dense peak"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+E2E_INFLIGHT = 3                 # end-to-end steps in flight (one stream each)
 
 
 def parse():
@@ -378,33 +379,74 @@ def gpu_arm(args, ws, rank, local):
     value = ws * step_flops / (ms / 1e3) / 1e12
 
     # ------------------------------------------------ end to end through host buffers
+    # Every step copies its Q, K, V in from pinned host memory, runs the
+    # whole path through the public API and reads O and lse back into pinned
+    # host memory.  E2E_INFLIGHT steps run at once, each on its own stream
+    # with its own device buffers, so one step's copies overlap another's
+    # kernels (a serving loop); the value is valid-pair FLOPs of all steps /
+    # the span from the first copy in to the last copy out.
     e2e = None
     if not args.no_e2e:
-        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        n_e2e = max(3, min(steps, 50))
+        nslot = E2E_INFLIGHT
+        slots = []
+        for _ in range(nslot):
+            sx = {"stream": torch.cuda.Stream(device=dev),
+                  "q": torch.empty_like(qd), "k": torch.empty_like(kd), "v": torch.empty_like(vd),
+                  "ws": torch.empty_like(wsbuf), "out": torch.empty_like(out), "lse": torch.empty_like(lse),
+                  "oh": torch.empty(out.shape, dtype=out.dtype, pin_memory=True),
+                  "lh": torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True),
+                  "split": [(s2, p2, torch.empty_like(b2), torch.empty_like(o2), torch.empty_like(l2))
+                            for s2, p2, b2, o2, l2 in split]}
+            if split:
+                sx["mout"], sx["mlse"] = torch.empty_like(mout), torch.empty_like(mlse)
+            slots.append(sx)
+
+        def e2e_step(sx):
+            with torch.cuda.stream(sx["stream"]):
+                sx["q"].copy_(qh, non_blocking=True)
+                sx["k"].copy_(kh, non_blocking=True)
+                sx["v"].copy_(vh, non_blocking=True)
+                t = pkg.attn_build_tiles(sl, w.S, w.S, ws=sx["ws"], prepared=prep)
+                pkg.attn_fwd(sx["q"], sx["k"], sx["v"], t, w.scale, out=sx["out"], lse=sx["lse"])
+                res, resl = sx["out"], sx["lse"]
+                if split:
+                    parts = []
+                    for s2, p2, b2, o2, l2 in sx["split"]:
+                        t2 = pkg.attn_build_tiles(s2, w.S, w.S, ws=b2, prepared=p2)
+                        pkg.attn_fwd(sx["q"], sx["k"], sx["v"], t2, w.scale, out=o2, lse=l2)
+                        parts.append((o2, l2))
+                    pkg.attn_merge([x[0] for x in parts], [x[1] for x in parts], out=sx["mout"], lse=sx["mlse"])
+                    res, resl = sx["mout"], sx["mlse"]
+                sx["oh"].copy_(res, non_blocking=True)
+                sx["lh"].copy_(resl, non_blocking=True)
+
+        for i in range(2 * nslot):                       # warm-up
+            e2e_step(slots[i % nslot])
+        torch.cuda.synchronize()
+        n_e2e = max(3 * nslot, min(steps, 48))
         es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        tot = 0.0
-        for i in range(n_e2e + 2):
-            flush.zero_()
-            es.record(stream)
-            qx = qh.to(dev, non_blocking=True)
-            kx = kh.to(dev, non_blocking=True)
-            vx = vh.to(dev, non_blocking=True)
-            step(qx, kx, vx)
-            res = mout if split else out
-            resl = mlse if split else lse
-            oh.copy_(res, non_blocking=True)
-            lh.copy_(resl, non_blocking=True)
-            ee.record(stream)
-            ee.synchronize()
-            if i >= 2:
-                tot += es.elapsed_time(ee)
-        e2e_ms = reduce_max(tot / n_e2e, ws, dev)
+        barrier(ws)
+        torch.cuda.synchronize()
+        es.record(stream)
+        for sx in slots:
+            sx["stream"].wait_event(es)
+        for i in range(n_e2e):
+            e2e_step(slots[i % nslot])
+        for sx in slots:
+            stream.wait_stream(sx["stream"])
+        ee.record(stream)
+        ee.synchronize()
+        barrier(ws)
+        rc = pkg.attn_last_device_error()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} in the end-to-end region")
+        e2e_ms = reduce_max(es.elapsed_time(ee) / n_e2e, ws, dev)
         h2d = (q.numel() + k.numel() + v.numel()) * 2 + sum(int(x[1]) * 20 for x in [prep] + [s[1] for s in split])
         d2h = out.numel() * 2 + lse.numel() * 4
         e2e = {"value": ws * step_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps_in_flight": nslot, "steps": n_e2e,
+               "l2": "not flushed: each step copies its inputs in from the host"}
 
     pk, pk_src = peaks()
     fwd_s = fwd_mean / 1e3
