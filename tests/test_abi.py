@@ -73,6 +73,11 @@ def test_workspace_bound_and_argument_checks(lib):
                               ctypes.byref(st), None)
     assert rc == B.ATTN_ERR_OVERLAP
     assert lib.attn_strerror(B.ATTN_ERR_TIMEOUT).decode().startswith("a bounded")
+    # exponential mode: only periods 0, 4 and 8 exist (host-side setting)
+    for bad in (-1, 1, 2, 3, 16):
+        assert lib.attn_set_exp2_poly(bad) == B.ATTN_ERR_INVALID_ARG
+    for good in (4, 8, 0):
+        assert lib.attn_set_exp2_poly(good) == B.ATTN_OK
 
 
 def _brute_overlap(sl):
