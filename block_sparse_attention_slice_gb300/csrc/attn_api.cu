@@ -89,7 +89,8 @@ WsLayout layout(const attn_slice_t *s, int n, int nq, int nk, int tq, int tk) {
   L.slices = 0;
   L.qb_ptr = sizeof(attn_slice_t) * n;
   L.qb_idx = L.qb_ptr + sizeof(int32_t) * (nq + 1);
-  L.input_bytes = L.qb_idx + sizeof(int32_t) * touched_q;
+  L.gbar = L.qb_idx + sizeof(int32_t) * touched_q;
+  L.input_bytes = L.gbar + sizeof(int32_t);
   size_t o = up(L.input_bytes);
   auto put = [&](size_t bytes) {
     const size_t at = o;
@@ -205,6 +206,8 @@ int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
   b.nref_q = reinterpret_cast<int32_t *>(ws + L.nref_q);
   b.ref_base_q = reinterpret_cast<int32_t *>(ws + L.ref_base_q);
   b.pairs_q = reinterpret_cast<int64_t *>(ws + L.pairs_q);
+  b.grid_bar = reinterpret_cast<int32_t *>(ws + L.gbar);
+  b.wait_ns = attn::wait_limit_ns();
   b.row_ptr = t.row_ptr;
   b.col_idx = t.col_idx;
   b.pairs = t.pairs;

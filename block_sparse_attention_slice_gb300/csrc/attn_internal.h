@@ -12,8 +12,9 @@ namespace attn {
 // Host-side checks and workspace layout of the tile metadata (attn_api.cu).
 namespace host {
 struct WsLayout {
-  // input region (one upload): slices | qb_ptr | qb_idx, then the outputs
-  size_t slices, qb_ptr, qb_idx, input_bytes;
+  // input region (one upload): slices | qb_ptr | qb_idx | grid barrier word
+  // (uploaded as 0), then the outputs
+  size_t slices, qb_ptr, qb_idx, gbar, input_bytes;
   size_t row_ptr, sched, nnz_q, nref_q, ref_base_q, pairs_q, totals, col_idx, pairs, ref_ptr,
       kind, ref_idx, total;
   int64_t cap_e, cap_r, n_qb;
@@ -38,6 +39,8 @@ struct BuildLaunch {
   uint8_t *kind;
   int64_t *totals;
   int64_t cap_entries, cap_refs;
+  int32_t *grid_bar;                // zero at launch (part of the uploaded input region)
+  unsigned long long wait_ns;       // bound of the single-launch build's grid barrier
 };
 
 int build_tiles_launch(const BuildLaunch &b, cudaStream_t s);

@@ -13,7 +13,9 @@
 //   MASKED  (otherwise)        -> references the slices with pairs in it
 // (UltraAttn page, section 3: Full / Causal / Empty blocks).
 //
-// Two launches on one stream:
+// One cooperative launch (both phases, a grid-wide barrier between them)
+// when every query tile's CTA fits on the GPU at once, else two launches on
+// one stream:
 //   count  one CTA per query tile: per-key-tile counts in shared memory ->
 //          entries, references and pairs of the query tile; the slices
 //          visited are the query tile's bucket (built on the host with the
@@ -32,8 +34,10 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "attn_internal.h"
+#include "ptx.cuh"
 
 namespace attn {
 
@@ -167,10 +171,9 @@ __device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(BT) count_kernel(const BuildLaunch b) {
-  extern __shared__ int shm[];
-  int *cnt = shm, *nref = shm + b.nk, *sh = shm + 2 * b.nk;
-  const int qt = blockIdx.x;
+// Count phase of query tile qt: per-key-tile counts (cnt, nref, kept in
+// shared memory) -> the tile's entries, references and pairs.
+__device__ void count_phase(const BuildLaunch &b, int qt, int *cnt, int *nref, int *sh) {
   count_tile_row(b, qt, cnt, nref);
   const int full = b.tq * b.tk;
   int e = 0, r = 0;
@@ -200,11 +203,14 @@ __global__ void __launch_bounds__(BT) count_kernel(const BuildLaunch b) {
   }
 }
 
-__global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
-  extern __shared__ int shm[];
-  int *cnt = shm, *nref = shm + b.nk, *rpos = shm + 2 * b.nk, *sh = shm + 3 * b.nk;
-  const int qt = blockIdx.x;
-  const int w = b.nnz_q[qt];
+// Fill phase of query tile qt: offsets (sums over the preceding query
+// tiles), the longest-processing-time rank, then the tile's entries in
+// ascending key-tile order and its slice references.  `recount` recomputes
+// cnt / nref (two-launch path); the single-launch path still has them.
+// The per-tile counters of other CTAs are read through L2 (__ldcg).
+__device__ void fill_phase(const BuildLaunch &b, int qt, int *cnt, int *nref, int *rpos, int *sh,
+                           bool recount) {
+  const int w = __ldcg(b.nnz_q + qt);
 
   // offsets of this query tile (sums over the preceding ones), and the
   // longest-processing-time rank: tiles with more entries first, ties broken
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
   long long e_before = 0, r_before = 0, e_all = 0, r_all = 0, p_all = 0;
   int rank = 0;
   for (int j = threadIdx.x; j < b.nq; j += BT) {
-    const int wj = b.nnz_q[j], rj = b.nref_q[j];
+    const int wj = __ldcg(b.nnz_q + j), rj = __ldcg(b.nref_q + j);
     rank += (wj > w || (wj == w && j < qt)) ? 1 : 0;
     if (j < qt) {
       e_before += wj;
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
     if (qt == 0) {
       e_all += wj;
       r_all += rj;
-      p_all += b.pairs_q[j];
+      p_all += __ldcg(reinterpret_cast<const long long *>(b.pairs_q) + j);
     }
   }
   __shared__ long long red[6][BT / 32];
@@ -254,9 +260,9 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
     }
   }
   // capacity exceeded: leave this tile's lists unwritten (the status says so)
-  if (row_start + w > b.cap_entries || ref_start + b.nref_q[qt] > b.cap_refs) return;
+  if (row_start + w > b.cap_entries || ref_start + __ldcg(b.nref_q + qt) > b.cap_refs) return;
 
-  count_tile_row(b, qt, cnt, nref);
+  if (recount) count_tile_row(b, qt, cnt, nref);
   const int full = b.tq * b.tk;
   // entries of this query tile in ascending key-tile order: each thread owns
   // a contiguous run of key tiles so a single scan orders them
@@ -284,8 +290,6 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
     if (masked) rbase += nref[t];
   }
   __syncthreads();
-  // slice references of MASKED tiles, ascending slice id: slices are visited
-  // in ascending order and each key tile is written by one thread per slice
   // slice references of MASKED tiles: one warp per key tile walks the
   // bucket in ascending slice id, so each list comes out ordered
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
@@ -307,24 +311,99 @@ __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
   }
 }
 
+__global__ void __launch_bounds__(BT) count_kernel(const BuildLaunch b) {
+  extern __shared__ int shm[];
+  count_phase(b, blockIdx.x, shm, shm + b.nk, shm + 2 * b.nk);
+}
+
+__global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
+  extern __shared__ int shm[];
+  fill_phase(b, blockIdx.x, shm, shm + b.nk, shm + 2 * b.nk, shm + 3 * b.nk, true);
+}
+
+// Both phases in one cooperative launch (every CTA resident): the counts
+// stay in shared memory across a grid-wide barrier, so nothing is
+// recounted and one launch is saved.  The barrier counter starts at 0 (it is
+// part of the uploaded input region).  Its wait is bounded: a CTA that gives
+// up records ATTN_ERR_TIMEOUT in the totals' status and poisons the counter,
+// and every CTA that sees the poison (CTA 0 included, which would otherwise
+// write the status) skips the fill.
+constexpr int kBarrierPoison = 1 << 30;
+
+__global__ void __launch_bounds__(BT) build_kernel(const BuildLaunch b) {
+  extern __shared__ int shm[];
+  int *cnt = shm, *nref = shm + b.nk, *rpos = shm + 2 * b.nk, *sh = shm + 3 * b.nk;
+  const int qt = blockIdx.x;
+  count_phase(b, qt, cnt, nref, sh);
+  __shared__ int arrived;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();                   // this tile's counters before the arrival
+    atomicAdd(b.grid_bar, 1);
+    const unsigned long long deadline = globaltimer_ns() + b.wait_ns;
+    int v;
+    while ((v = *reinterpret_cast<volatile int *>(b.grid_bar)) < static_cast<int>(gridDim.x)) {
+      if (globaltimer_ns() > deadline) {
+        atomicAdd(b.grid_bar, kBarrierPoison);
+        atomicExch(reinterpret_cast<unsigned long long *>(b.totals + 3),
+                   static_cast<unsigned long long>(ATTN_ERR_TIMEOUT));
+        v = kBarrierPoison;
+        break;
+      }
+    }
+    __threadfence();
+    arrived = v < kBarrierPoison;
+  }
+  __syncthreads();
+  if (!arrived) return;
+  fill_phase(b, qt, cnt, nref, rpos, sh, false);
+}
+
 int build_tiles_launch(const BuildLaunch &b, cudaStream_t s) {
   const size_t sm_count = (2 * static_cast<size_t>(b.nk) + 64) * sizeof(int);
   const size_t sm_fill = (3 * static_cast<size_t>(b.nk) + 64) * sizeof(int);
-  static int configured_dev = -1;
+  constexpr int kMaxDev = 64;
+  static int coresident[kMaxDev] = {};   // CTAs of build_kernel that fit at once, per device
+  static size_t coresident_smem[kMaxDev] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
+  static bool configured[kMaxDev] = {};
+  if (!configured[dev]) {
     if (cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              200 * 1024) != cudaSuccess ||
         cudaFuncSetAttribute(fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             200 * 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              200 * 1024) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    configured_dev = dev;
+    configured[dev] = true;
   }
-  if (b.nq > 0) {
-    count_kernel<<<b.nq, BT, sm_count, s>>>(b);
-    fill_kernel<<<b.nq, BT, sm_fill, s>>>(b);
+  if (b.nq <= 0) return ATTN_OK;
+  // one launch when every query tile's CTA can be resident at once
+  if (coresident_smem[dev] != sm_fill) {
+    int per_sm = 0, sms = 0, coop = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_kernel, BT, sm_fill) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    coresident[dev] = coop ? per_sm * sms : 0;
+    coresident_smem[dev] = sm_fill;
   }
+  // ATTN_BUILD_TWO_LAUNCH=1 in the environment selects the two-launch path
+  // (used by the tests to check that both paths give the same metadata)
+  const char *two = std::getenv("ATTN_BUILD_TWO_LAUNCH");
+  const bool force_two = two && two[0] == '1';
+  if (!force_two && b.nq <= coresident[dev]) {
+    BuildLaunch arg = b;
+    void *args[] = {&arg};
+    if (cudaLaunchCooperativeKernel(reinterpret_cast<void *>(build_kernel), dim3(b.nq), dim3(BT),
+                                    args, sm_fill, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  count_kernel<<<b.nq, BT, sm_count, s>>>(b);
+  fill_kernel<<<b.nq, BT, sm_fill, s>>>(b);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

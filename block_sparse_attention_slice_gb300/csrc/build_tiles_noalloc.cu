@@ -112,6 +112,8 @@ extern "C" int attn_build_tiles_noalloc(const attn_slice_t *h_slices, int n_slic
   b.nref_q = reinterpret_cast<int32_t *>(sc + 4 * static_cast<size_t>(attn::kMaxQTiles));
   b.ref_base_q = reinterpret_cast<int32_t *>(sc + 8 * static_cast<size_t>(attn::kMaxQTiles));
   b.pairs_q = reinterpret_cast<int64_t *>(sc + 12 * static_cast<size_t>(attn::kMaxQTiles));
+  b.grid_bar = reinterpret_cast<int32_t *>(ws + L.gbar);
+  b.wait_ns = attn::wait_limit_ns();
   b.row_ptr = t.row_ptr;
   b.col_idx = t.col_idx;
   b.pairs = t.pairs;

@@ -67,3 +67,21 @@ def test_rebuild_is_identical():
     b = attn_build_tiles(sl, 3000, 3000, 256, 128).to_host()
     for key in KEYS:
         assert np.array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("seed,sq,sk,tq,tk", [
+    (11, 1000, 1100, 256, 128), (12, 3000, 2500, 64, 64), (13, 160, 176, 8, 8)])
+def test_single_and_two_launch_builds_agree(seed, sq, sk, tq, tk, monkeypatch):
+    # the build runs as one cooperative launch when every query tile's CTA
+    # fits on the GPU at once, else as two launches; both must give the
+    # oracle's metadata bit for bit
+    sl = W.random_slices(sq, sk, 24, seed=seed, unit=1, max_len=max(8, min(sq, sk) // 3))
+    ref = oracle.oracle_tiles(sl, sq, sk, tq, tk)
+    monkeypatch.delenv("ATTN_BUILD_TWO_LAUNCH", raising=False)
+    one = attn_build_tiles(sl, sq, sk, tq, tk).to_host()
+    monkeypatch.setenv("ATTN_BUILD_TWO_LAUNCH", "1")
+    two = attn_build_tiles(sl, sq, sk, tq, tk).to_host()
+    for key in KEYS:
+        assert np.array_equal(one[key], ref[key]), key
+        assert np.array_equal(two[key], ref[key]), key
+    assert one["total_pairs"] == two["total_pairs"] == ref["total_pairs"]
