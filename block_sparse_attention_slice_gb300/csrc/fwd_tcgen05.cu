@@ -63,8 +63,11 @@ constexpr int IQ = 4;             // queued work-item ids
 constexpr int SCHED_SLOTS = 4096; // work counters, one per launch in flight
 
 // Work counters of forward launches: each launch takes the next slot (host
-// side, round robin) and zeroes it on its stream before the kernel runs.
-__device__ unsigned int g_sched_counter[SCHED_SLOTS];
+// side, round robin).  Slot i holds the item counter at [i] and the count of
+// retired CTAs at [SCHED_SLOTS + i]; both start at 0 (static device memory)
+// and the launch's last CTA to retire puts both back to 0, so no launch needs
+// a memset before it.
+__device__ unsigned int g_sched_counter[2 * SCHED_SLOTS];
 
 struct FwdParams {
   const int32_t *row_ptr, *col_idx, *ref_ptr, *ref_idx, *sched;
@@ -76,7 +79,7 @@ struct FwdParams {
   int out_f32;                    // f32 O by direct stores, else bf16 O by TMA stores
   float scale_log2;               // scale * log2(e)
   unsigned long long wait_ns;
-  unsigned int *counter;          // this launch's work counter (zeroed before launch)
+  unsigned int *counter;          // this launch's work counter (0 at launch, reset by its last CTA)
 };
 
 // One resolved tile entry: key tile, kind, reference range and up to two
@@ -627,7 +630,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 9) tmem_dealloc(tmem, 512);
-  if (threadIdx.x == 0 && *abort) atomicExch(&g_fwd_status, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
+  if (threadIdx.x == 0) {
+    if (*abort) atomicExch(&g_fwd_status, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
+    // every CTA has fetched its last item id once it gets here: the last one
+    // to retire resets this launch's slot for its next use
+    __threadfence();
+    if (atomicAdd(p.counter + SCHED_SLOTS, 1u) == gridDim.x - 1) {
+      atomicExch(p.counter, 0u);
+      atomicExch(p.counter + SCHED_SLOTS, 0u);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -712,8 +724,7 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   if (sms <= 0) return ATTN_ERR_CUDA;
   const int grid = static_cast<int>(items < sms ? items : sms);
   p.counter = next_counter();
-  if (!p.counter || cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  if (!p.counter) return ATTN_ERR_CUDA;
   const int poly = g_exp2_poly;
   if (d == 128) {
     if (poly == 4) return launch_fwd<128, 4, 4>(mq, mk, mv, mo, p, grid, stream);
