@@ -312,7 +312,10 @@ def gpu_arm(args, ws, rank, local):
     nnz, nref, pairs_per_head, status = tiles0.totals()
     assert status == 0
     flops = 4.0 * w.d * pairs_per_head * w.H
-    launches_per_step = 3 + 1 + (len(split) * 4 + 1 if split else 0)
+    # kernels per step: the metadata build (one cooperative launch on these
+    # workloads: every query tile's CTA fits at once) and the forward, for
+    # the whole problem and for each KV-split part, plus the merge
+    launches_per_step = 2 + (len(split) * 2 + 1 if split else 0)
 
     def step(qx, kx, vx, ev=None):
         if ev is not None:
@@ -547,7 +550,7 @@ def bwd_arm(args, ws, rank, local):
             "roofline": {"kernel": "attn_bwd", "bound": "tensor", "achieved": val,
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": val / pk["bf16_tflops"],
                          "traffic": None, "peak_source": f"bf16_tflops (burst) of {pk_src}"},
-            "gpu_launches": 6 * steps, "clocks": clk}), flush=True)
+            "gpu_launches": 5 * steps, "clocks": clk}), flush=True)   # delta, 2 x transposed lists, dK/dV, dQ
 
 
 def main():
