@@ -5,7 +5,8 @@ split, packed varlen causal documents, a block-sparse strided grid, a
 video-generation slice list, a long GQA causal problem with an 8-way KV
 split), plus fuzzed slice lists over all four slice kinds with ragged sizes,
 both head dims, grouped heads, closed-form uniform-score cases and an
-Empty-tile poisoning check.
+Empty-tile poisoning check and a head-dim-64 problem with many work items
+per CTA.
 """
 import math
 
@@ -106,6 +107,20 @@ def test_long_gqa_causal_whole_and_kv_split_sampled():
     compare(mo, ml, ref)
 
 
+def test_d64_varlen_many_items_per_cta():
+    # head dim 64 on the packed-document workload with 4 query heads per KV
+    # head: 1024 work items, so every CTA runs several items back to back
+    # with row lengths from 2 to 16 key tiles
+    import dataclasses
+    w = dataclasses.replace(W.varlen_causal(), name="varlen_causal_s16384_h16_hk4_d64",
+                            Hk=4, d=64, scale=0.125)
+    q, k, v, qd, kd, vd = _qkv(w)
+    out, lse = _fwd_checked(qd, kd, vd, attn_build_tiles(w.slices, w.S, w.S), w.scale)
+    extra = [0, 127, 128, 255, 256, w.S - 1] + [int(x) for s in w.slices for x in (s[0], s[1] - 1)]
+    rows = rows_per_head(w, n=512, extra=extra)
+    compare(out, lse, run_oracle(q, k, v, w.scale, mask_fn(w), rows=rows))
+
+
 @pytest.mark.parametrize("seed,sq,sk,H,Hk,d", [
     (0, 512, 512, 2, 1, 128), (1, 1000, 1100, 4, 2, 64), (2, 700, 1300, 2, 2, 128),
     (3, 1300, 600, 3, 1, 64), (4, 2304, 2304, 2, 2, 128), (5, 129, 257, 1, 1, 128)])
@@ -124,11 +139,12 @@ def test_fuzzed_slices_all_kinds(seed, sq, sk, H, Hk, d):
     compare(out, lse, ref)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("kind", [0, 1, 2, 3])
-def test_uniform_scores_give_means(kind):
+def test_uniform_scores_give_means(kind, d):
     # q = 0: every score is 0, so P = 1 exactly and O is the mean of V over
     # the valid keys (closed form), lse = ln(count).
-    S, d = 640, 128
+    S = 640
     rng = np.random.default_rng(kind)
     q = torch.zeros((S, 1, d), dtype=torch.bfloat16)
     v = torch.from_numpy(rng.standard_normal((S, 1, d), dtype=np.float32)).to(torch.bfloat16)
