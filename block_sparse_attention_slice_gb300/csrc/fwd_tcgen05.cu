@@ -98,8 +98,8 @@ struct Layout {
   static constexpr int TILE = NHALF * HALF;          // 128 x D bf16
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TILE;
-  static constexpr int ST_OFF = KV_OFF + NS * TILE;   // bf16 O staging: one 128 x 64 half per tile
-  static constexpr int REC_OFF = ST_OFF + 2 * HALF;
+  static constexpr int ST_OFF = KV_OFF + NS * TILE;   // bf16 O staging: one 128 x D tile per MMA tile
+  static constexpr int REC_OFF = ST_OFF + 2 * TILE;
   static constexpr int IQ_OFF = REC_OFF + RING * 64;
   static constexpr int BAR_OFF = IQ_OFF + IQ * 16;
   // q_full | q_empty | full[NS] | empty[NS] | s_full[2] | p_full[2] | o_full[2] | drain |
@@ -403,6 +403,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + 256 + t * 128;
     const float sl2 = p.scale_log2;
+    const bool elected = wl == 0 && lane == 0;   // issues this tile's output stores
+    bool ee_due = false;   // elected: the last stores' staging release is not yet signalled
     uint32_t step = 0, rpos = 0, nonempty = 0, ep = 0;
     bool ok = true;
     uint32_t qpos = 0;
@@ -537,6 +539,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::B_P + t));
+        if (ee_due) {
+          // a KV step after the last item's stores were issued: they have read
+          // the staging by now, normally without waiting
+          bulk_wait_read_all();
+          mbar_arrive(bar(L::B_EE + t));
+          ee_due = false;
+        }
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -550,20 +559,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (!p.out_f32) {
-        // bf16 O through a 128 x 64 shared-memory half in the 128-byte
-        // swizzle of the output's tensor map (16-byte chunk c of row r at
-        // chunk c ^ (r & 7)), one TMA store per half; the store clips the
-        // rows past S_q
-        const uint32_t stg = sb + L::ST_OFF + t * L::HALF;
+        // bf16 O through this tile's 128 x D shared-memory staging, each
+        // 64-column half in the 128-byte swizzle of the output's tensor map
+        // (16-byte chunk c of row r at chunk c ^ (r & 7)), one TMA store per
+        // half; the store clips the rows past S_q.  Nothing here waits for
+        // the stores: the elected thread confirms that they have read the
+        // staging during the next item's first KV step (or at the next
+        // epilogue, if that comes first).
+        const uint32_t stg = sb + L::ST_OFF + t * L::TILE;
         const int r = wl * 32 + lane;
-        const bool elected = wl == 0 && lane == 0;
         const int y0 = it.qt * 256 + t * BM;
-        for (int hh = 0; hh < L::NHALF; ++hh) {
-          // the previous store out of this half has finished reading it
-          if (ep > 0 && !wait_all(bar(L::B_EE + t), (ep - 1) & 1, abort, lim)) {
+        if (ep > 0) {
+          if (ee_due) {
+            bulk_wait_read_all();
+            mbar_arrive(bar(L::B_EE + t));
+            ee_due = false;
+          }
+          if (!wait_all(bar(L::B_EE + t), (ep - 1) & 1, abort, lim)) {
             ok = false;
             break;
           }
+        }
+#pragma unroll 1
+        for (int hh = 0; hh < L::NHALF; ++hh) {
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
             uint32_t x[32];
@@ -580,22 +598,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               v.y = pack_bf16x2(__uint_as_float(x[8 * q4 + 2]) * inv, __uint_as_float(x[8 * q4 + 3]) * inv);
               v.z = pack_bf16x2(__uint_as_float(x[8 * q4 + 4]) * inv, __uint_as_float(x[8 * q4 + 5]) * inv);
               v.w = pack_bf16x2(__uint_as_float(x[8 * q4 + 6]) * inv, __uint_as_float(x[8 * q4 + 7]) * inv);
-              st_shared_v4(stg + r * 128 + (((c2 * 4 + q4) ^ (r & 7)) << 4), v);
+              st_shared_v4(stg + hh * L::HALF + r * 128 + (((c2 * 4 + q4) ^ (r & 7)) << 4), v);
             }
           }
-          fence_proxy_async_smem();
-          mbar_arrive(bar(L::B_EF + t));
-          if (elected) {
-            if (mbar_wait_bounded(bar(L::B_EF + t), ep & 1, abort, lim) && y0 < p.sq) {
-              tma_store_2d(&tm_o, stg, it.h * D + hh * 64, y0);
-              bulk_commit_group();
-              bulk_wait_read_all();
-            }
-            mbar_arrive(bar(L::B_EE + t));
-          }
-          ++ep;
         }
-        if (!ok) break;
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::B_EF + t));
+        if (elected) {
+          if (mbar_wait_bounded(bar(L::B_EF + t), ep & 1, abort, lim) && y0 < p.sq) {
+            for (int hh = 0; hh < L::NHALF; ++hh)
+              tma_store_2d(&tm_o, stg + hh * L::HALF, it.h * D + hh * 64, y0);
+            bulk_commit_group();
+          }
+          ee_due = true;
+        }
+        ++ep;
       } else {
         // f32 O (KV-split partials): one thread per row, 16-byte stores
 #pragma unroll 1
@@ -727,9 +744,9 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   if (!p.counter) return ATTN_ERR_CUDA;
   const int poly = g_exp2_poly;
   if (d == 128) {
-    if (poly == 4) return launch_fwd<128, 4, 4>(mq, mk, mv, mo, p, grid, stream);
-    if (poly == 8) return launch_fwd<128, 4, 8>(mq, mk, mv, mo, p, grid, stream);
-    return launch_fwd<128, 4, 0>(mq, mk, mv, mo, p, grid, stream);
+    if (poly == 4) return launch_fwd<128, 3, 4>(mq, mk, mv, mo, p, grid, stream);
+    if (poly == 8) return launch_fwd<128, 3, 8>(mq, mk, mv, mo, p, grid, stream);
+    return launch_fwd<128, 3, 0>(mq, mk, mv, mo, p, grid, stream);
   }
   if (poly == 4) return launch_fwd<64, 8, 4>(mq, mk, mv, mo, p, grid, stream);
   if (poly == 8) return launch_fwd<64, 8, 8>(mq, mk, mv, mo, p, grid, stream);
