@@ -31,10 +31,12 @@
 //   PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1)
 // so the tensor core works on one tile while the softmax warps of the other
 // tile run (FlashAttention-4 page: softmax overlapped with the MMAs).
-// The epilogue of a bf16 output stages each 128 x 64 half of O_t / l in
-// shared memory (the 128-byte swizzle of the output's tensor map) and leaves
-// it with one TMA store, which writes whole rows and clips the rows past
-// S_q; f32 partial outputs keep one thread per row.
+// The epilogue of a bf16 output stages O_t / l in the tile's own 128 x D
+// shared-memory buffer (each 64-column half in the 128-byte swizzle of the
+// output's tensor map) and leaves it with one TMA store per half, which
+// writes whole rows and clips the rows past S_q; nothing waits for the
+// stores until the buffer is needed again.  f32 partial outputs keep one
+// thread per row.
 // tcgen05 operations of one thread complete in issue order, so when the
 // softmax of tile t sees S_t(j) its previous PV_t(j-1) has completed too,
 // and the next item's first QK may be issued while the softmax warps are

@@ -186,6 +186,34 @@ def test_empty_tiles_never_read():
     assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_mostly_empty_query_tiles(d):
+    # 28 of 32 query tiles have no key tile: with 48 heads that is 192
+    # non-empty and 1344 empty work items, the empty ones last in the LPT
+    # order, so CTAs run several items and meet runs of empty items right
+    # after their last non-empty one; those rows must come out as O = 0,
+    # lse = -inf.
+    sq, sk, H, Hk = 8192, 2048, 48, 16
+    rng = np.random.default_rng(11)
+    sl = np.array([[0, 256, 0, 2048, 0], [7936, 8192, 0, 1024, 1], [3000, 3100, 500, 700, 3]],
+                  np.int32)
+    q = torch.from_numpy(rng.standard_normal((sq, H, d), dtype=np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy(rng.standard_normal((sk, Hk, d), dtype=np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((sk, Hk, d), dtype=np.float32)).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    out, lse = _fwd_checked(q.cuda(), k.cuda(), v.cuda(), attn_build_tiles(sl, sq, sk), scale)
+    rows = [np.concatenate([np.arange(0, 300), np.arange(2990, 3110), np.arange(7900, 8192),
+                            np.arange(5000, 5010)])] * H
+    ref = oracle.oracle_attention(f64(q), f64(k), f64(v), scale,
+                                  lambda r: oracle.mask_rows(sl, r, sk), rows=rows)
+    compare(out, lse, ref)
+    empty = torch.ones(sq, dtype=torch.bool)
+    for a, b, *_ in sl:
+        empty[a:b] = False
+    assert torch.all(out.cpu()[empty] == 0)
+    assert torch.all(torch.isneginf(lse.cpu()[:, empty]))
+
+
 def test_repeat_runs_bit_identical():
     w = W.tiny_causal()
     q, k, v, qd, kd, vd = _qkv(w)
