@@ -48,26 +48,49 @@ struct BwdParams {
 };
 
 // ------------------------------------------------------------------ D = rowsum(dO * O)
+// One thread per 8 consecutive elements (one 16-byte load of dO, one or two
+// of O; rows are 16-byte aligned), D / 8 neighbouring lanes per row, summed
+// by shuffles within those lanes.
 template <int D, bool O_F32>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const void *out, const uint16_t *dout,
                                                          float *delta, int sq, int hq) {
-  constexpr int V = D / 32;
-  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= static_cast<long long>(sq) * hq) return;
-  const int h = static_cast<int>(w / sq), i = static_cast<int>(w % sq);
-  const size_t base = (static_cast<size_t>(i) * hq + h) * D + lane * V;
+  constexpr int TPR = D / 8;   // threads per row
+  static_assert(32 % TPR == 0, "a row's lanes share one warp");
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long r = t / TPR;   // row (i, h) at i * hq + h
+  const bool valid = r < static_cast<long long>(sq) * hq;
   float acc = 0.f;
+  if (valid) {
+    const size_t base = static_cast<size_t>(t) * 8;
+    const uint4 g = *reinterpret_cast<const uint4 *>(dout + base);
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+    float o[8];
+    if (O_F32) {
+      const float4 a = *reinterpret_cast<const float4 *>(static_cast<const float *>(out) + base);
+      const float4 b = *reinterpret_cast<const float4 *>(static_cast<const float *>(out) + base + 4);
+      o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+      o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    } else {
+      const uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(out) + base);
+      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
 #pragma unroll
-  for (int k = 0; k < V; ++k) {
-    const float g = __uint_as_float(static_cast<uint32_t>(dout[base + k]) << 16);
-    const float o = O_F32 ? static_cast<const float *>(out)[base + k]
-                          : __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(out)[base + k]) << 16);
-    acc = fmaf(g, o, acc);
+      for (int k = 0; k < 4; ++k) {
+        o[2 * k] = __uint_as_float(ow[k] << 16);
+        o[2 * k + 1] = __uint_as_float(ow[k] & 0xffff0000u);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc = fmaf(__uint_as_float(gw[k] << 16), o[2 * k], acc);
+      acc = fmaf(__uint_as_float(gw[k] & 0xffff0000u), o[2 * k + 1], acc);
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) delta[static_cast<size_t>(h) * sq + i] = acc;
+  for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (valid && (t % TPR) == 0) {
+    const int i = static_cast<int>(r / hq), h = static_cast<int>(r % hq);
+    delta[static_cast<size_t>(h) * sq + i] = acc;
+  }
 }
 
 // ------------------------------------------------------------------ transposed lists
@@ -736,8 +759,8 @@ int bwd_launch(const void *q, const void *k, const void *v, const void *out, int
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_ns = wait_limit_ns();
 
-  const long long warps = static_cast<long long>(sq) * hq;
-  const unsigned dgrid = static_cast<unsigned>((warps * 32 + 255) / 256);
+  const long long dthreads = static_cast<long long>(sq) * hq * (d / 8);
+  const unsigned dgrid = static_cast<unsigned>((dthreads + 255) / 256);
   const uint16_t *dob = static_cast<const uint16_t *>(dout);
   if (d == 128) {
     if (out_dtype == ATTN_DTYPE_F32) bwd_delta_kernel<128, true><<<dgrid, 256, 0, stream>>>(out, dob, delta, sq, hq);
