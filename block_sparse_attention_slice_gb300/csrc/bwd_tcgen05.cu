@@ -472,18 +472,67 @@ __global__ void __launch_bounds__(B_THREADS, 1)
 
 // ------------------------------------------------------------------ dQ per query tile
 // Work item: (query tile, head) as in the forward; the two 128-row halves in
-// turn.  Tensor memory: S [0,128)  dP [128,256)  dQ [256,256+D); dS (bf16)
-// overwrites the first 64 columns of S.
+// turn.  Tensor memory: S_a [0,128)  dP [128,256)  dQ [256,256+D)
+// S_b [384,512).  S of key tile j goes to S_a for even j, S_b for odd j, and
+// dS (bf16) overwrites the first 64 columns of that S.  The element-wise
+// warps read all of dP(j) first and say so (dp_read), so the tensor core
+// computes dP(j+1) and S(j+2) while they form dS(j).  MMA order per key
+// tile j: dP(j+1) after dp_read(j), dQ += dS(j) K_j after p_done(j), then
+// S(j+2) into the S block dQ has just read.
 template <int D, int NS>
 struct QLayout {
   using B = BLayout<D>;
   static constexpr int Q_OFF = 0, DO_OFF = B::TILE, KV_OFF = 2 * B::TILE;
   static constexpr int BAR_OFF = KV_OFF + NS * B::TILE;
+  // q_full | q_empty | full[NS] | empty[NS] | s_full | p_done | o_full | drain | dp_read
   static constexpr int B_Q = 0, B_QE = 1, B_FULL = 2, B_EMPTY = 2 + NS, B_S = 2 + 2 * NS,
-                       B_P = B_S + 1, B_O = B_P + 1, B_DR = B_O + 1, NBAR = B_DR + 1;
+                       B_P = B_S + 1, B_O = B_P + 1, B_DR = B_O + 1, B_DPR = B_DR + 1,
+                       NBAR = B_DPR + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int ALLOC = MISC_OFF + 16 + 1024;
+  static_assert(ALLOC <= 232448, "shared memory per CTA");
 };
+
+// Column block of S(j) in the dQ kernel's tensor memory.
+__device__ __forceinline__ uint32_t q_s_col(int j) { return (j & 1) ? 384u : 0u; }
+
+// The dQ kernel's element-wise step for one query row: all 128 columns of dP
+// into registers first (then dp_read), then S in 32-column chunks; dS =
+// P (dP - D) with P = exp2(S scale log2e - lse2) on the valid columns goes
+// back over the first 64 columns of S as bf16 pairs.
+__device__ __forceinline__ void ds_step_dp_first(uint32_t t_s, uint32_t t_dp, const uint32_t (&w)[4],
+                                                 float sl2, float lse2, float dlt, uint32_t dp_read) {
+  uint32_t y[128];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld32(t_dp + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&y[c * 32]));
+  tmem_wait_ld();
+#pragma unroll
+  for (int k = 0; k < 128; ++k) asm volatile("" : "+r"(y[k]));
+  tc_fence_before();
+  mbar_arrive(dp_read);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t x[32];
+    tmem_ld32(t_s + c * 32, x);
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) asm volatile("" : "+r"(x[k]));
+    uint32_t dk[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      float dv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int col = c * 32 + 2 * k + u;
+        const bool ok = (w[col >> 5] >> (col & 31)) & 1u;
+        const float e = ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), sl2, -lse2));
+        dv[u] = ok ? e * (__uint_as_float(y[col]) - dlt) : 0.f;
+      }
+      dk[k] = pack_bf16x2(dv[0], dv[1]);
+    }
+    tmem_st16(t_s + c * 16, dk);
+  }
+}
 
 template <int D, int NS>
 __global__ void __launch_bounds__(B_THREADS, 1)
@@ -519,6 +568,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     mbar_init(bar(L::B_P), 128);
     mbar_init(bar(L::B_O), 1);
     mbar_init(bar(L::B_DR), 1);
+    mbar_init(bar(L::B_DPR), 128);
     *abort = 0;
     fence_mbar_init();
   }
@@ -571,50 +621,86 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 1);
       const uint32_t qs = sb + L::Q_OFF, dos = sb + L::DO_OFF;
+      auto slot = [=](uint32_t pos) -> uint32_t { return sb + L::KV_OFF + (pos % NS) * BL::TILE; };
+      auto full = [=](uint32_t pos) -> bool {
+        return mbar_wait_bounded(bar(L::B_FULL + pos % NS), (pos / NS) & 1, abort, lim);
+      };
+      // S(j) = Q K^T and dP = dO V^T (SS); dQ += dS(j) K (TS, K MN-major)
+      auto mma_s = [=](int j, uint32_t kb) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
+          mma_ss(tmem + q_s_col(j), smem_desc_sw128(qs + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                 IDESC_QK, kk > 0);
+        }
+      };
+      auto mma_dp = [=](uint32_t vb) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
+          mma_ss(tmem + 128, smem_desc_sw128(dos + off, 16, 1024), smem_desc_sw128(vb + off, 16, 1024),
+                 IDESC_QK, kk > 0);
+        }
+      };
+      auto mma_dq = [=](int j, uint32_t kb) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + 256, tmem + q_s_col(j) + kk * 8, smem_desc_sw128(kb + kk * 16 * 128, BL::HALF, 1024),
+                 IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      // ring positions of a half: K_j at ld + 2j, V_j at ld + 2j + 1
       uint32_t ld = 0, s = 0;
       bool ok = true;
       for (int t = 0; ok && t < halves; ++t) {
-        if (!mbar_wait_bounded(bar(L::B_Q), t & 1, abort, lim)) {
-          ok = false;
-          break;
-        }
-        for (int j = 0; j < n; ++j, ld += 2, ++s) {
-          const uint32_t kpos = ld, vpos = ld + 1;
-          const uint32_t kb = sb + L::KV_OFF + (kpos % NS) * BL::TILE;
-          const uint32_t vb = sb + L::KV_OFF + (vpos % NS) * BL::TILE;
-          if (!mbar_wait_bounded(bar(L::B_FULL + kpos % NS), (kpos / NS) & 1, abort, lim) ||
-              !mbar_wait_bounded(bar(L::B_FULL + vpos % NS), (vpos / NS) & 1, abort, lim)) {
+        ok = mbar_wait_bounded(bar(L::B_Q), t & 1, abort, lim) && full(ld) && full(ld + 1);
+        if (!ok) break;
+        tc_fence_after();
+        mma_s(0, slot(ld));
+        mma_dp(slot(ld + 1));
+        mma_commit(bar(L::B_S));
+        mma_commit(bar(L::B_EMPTY + (ld + 1) % NS));
+        if (n == 1) mma_commit(bar(L::B_QE));
+        if (n > 1) {
+          if (!full(ld + 2)) {
             ok = false;
             break;
           }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
-            mma_ss(tmem, smem_desc_sw128(qs + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                   IDESC_QK, kk > 0);
+          mma_s(1, slot(ld + 2));
+        }
+        for (int j = 0; j < n; ++j, ++s) {
+          const uint32_t kj = ld + 2u * j;
+          if (j + 1 < n) {
+            // dP(j+1) once dP(j) is in the element-wise warps' registers;
+            // this commit also covers S(j+1), issued one key tile earlier
+            if (!full(kj + 3) || !mbar_wait_bounded(bar(L::B_DPR), s & 1, abort, lim)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            mma_dp(slot(kj + 3));
+            mma_commit(bar(L::B_S));
+            mma_commit(bar(L::B_EMPTY + (kj + 3) % NS));
+            if (j + 2 == n) mma_commit(bar(L::B_QE));   // the half's last reads of Q and dO
           }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
-            mma_ss(tmem + 128, smem_desc_sw128(dos + off, 16, 1024), smem_desc_sw128(vb + off, 16, 1024),
-                   IDESC_QK, kk > 0);
-          }
-          mma_commit(bar(L::B_S));
-          mma_commit(bar(L::B_EMPTY + vpos % NS));
-          if (j == n - 1) mma_commit(bar(L::B_QE));
           if (!mbar_wait_bounded(bar(L::B_P), s & 1, abort, lim)) {
             ok = false;
             break;
           }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + 256, tmem + kk * 8, smem_desc_sw128(kb + kk * 16 * 128, BL::HALF, 1024),
-                   IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(L::B_EMPTY + kpos % NS));
+          mma_dq(j, slot(kj));
+          mma_commit(bar(L::B_EMPTY + kj % NS));
+          if (j + 2 < n) {
+            if (!full(kj + 4)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            mma_s(j + 2, slot(kj + 4));
+          }
         }
         if (ok) mma_commit(bar(L::B_O));
+        ld += 2u * n;
       }
       mma_commit(bar(L::B_DR));
       wait_drain(bar(L::B_DR), 0, 20000000ull);
@@ -646,8 +732,8 @@ __global__ void __launch_bounds__(B_THREADS, 1)
           break;
         }
         tc_fence_after();
-        p_ds_step(tmem + lane_off, tmem + lane_off + 128, -1, 0, w, sl2,
-                  [&](int) { return lse2; }, [&](int) { return dlt; });
+        ds_step_dp_first(tmem + lane_off + q_s_col(j), tmem + lane_off + 128, w, sl2, lse2, dlt,
+                         bar(L::B_DPR));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::B_P));
@@ -694,7 +780,7 @@ static int set_smem(KernelT k, int bytes) {
 
 template <int D>
 static int launch_bwd_main(const CUtensorMap *m, const BwdParams &p, cudaStream_t s) {
-  constexpr int NS = D == 128 ? 4 : 8;
+  constexpr int NS = D == 128 ? 5 : 8;   // the dQ kernel's K/V ring
   int rc;
   if ((rc = set_smem(bwd_kv_kernel<D>, KVLayout<D>::ALLOC)) != ATTN_OK) return rc;
   if ((rc = set_smem(bwd_q_kernel<D, NS>, QLayout<D, NS>::ALLOC)) != ATTN_OK) return rc;
