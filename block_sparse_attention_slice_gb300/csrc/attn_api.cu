@@ -85,12 +85,11 @@ WsLayout layout(const attn_slice_t *s, int n, int nq, int nk, int tq, int tk) {
   L.cap_e = std::min<int64_t>(touched, static_cast<int64_t>(nq) * nk);
   L.cap_r = touched;
   L.n_qb = touched_q;
-  // input region: packed back to back (one upload), 4-byte aligned parts
+  // input region: packed back to back (one image), 4-byte aligned parts
   L.slices = 0;
   L.qb_ptr = sizeof(attn_slice_t) * n;
   L.qb_idx = L.qb_ptr + sizeof(int32_t) * (nq + 1);
-  L.gbar = L.qb_idx + sizeof(int32_t) * touched_q;
-  L.input_bytes = L.gbar + sizeof(int32_t);
+  L.input_bytes = L.qb_idx + sizeof(int32_t) * touched_q;
   size_t o = up(L.input_bytes);
   auto put = [&](size_t bytes) {
     const size_t at = o;
@@ -189,8 +188,6 @@ int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
 
   std::vector<uint8_t> img;
   stage_inputs(h_slices, n_slices, nq, tile_q, L, &img);
-  if (cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return ATTN_ERR_CUDA;
   attn::BuildLaunch b;
   b.slices = t.slices;
   b.qb_ptr = reinterpret_cast<const int32_t *>(ws + L.qb_ptr);
@@ -206,7 +203,8 @@ int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
   b.nref_q = reinterpret_cast<int32_t *>(ws + L.nref_q);
   b.ref_base_q = reinterpret_cast<int32_t *>(ws + L.ref_base_q);
   b.pairs_q = reinterpret_cast<int64_t *>(ws + L.pairs_q);
-  b.grid_bar = reinterpret_cast<int32_t *>(ws + L.gbar);
+  b.off_qb_ptr = static_cast<uint32_t>(L.qb_ptr);
+  b.off_qb_idx = static_cast<uint32_t>(L.qb_idx);
   b.wait_ns = attn::wait_limit_ns();
   b.row_ptr = t.row_ptr;
   b.col_idx = t.col_idx;
@@ -218,7 +216,7 @@ int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
   b.totals = t.totals;
   b.cap_entries = L.cap_e;
   b.cap_refs = L.cap_r;
-  if ((rc = attn::build_tiles_launch(b, s)) != ATTN_OK) return rc;
+  if ((rc = attn::build_tiles_launch(b, img.data(), img.size(), ws, s)) != ATTN_OK) return rc;
   *tiles = t;
   return ATTN_OK;
 }

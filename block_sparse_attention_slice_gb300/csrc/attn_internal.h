@@ -12,9 +12,8 @@ namespace attn {
 // Host-side checks and workspace layout of the tile metadata (attn_api.cu).
 namespace host {
 struct WsLayout {
-  // input region (one upload): slices | qb_ptr | qb_idx | grid barrier word
-  // (uploaded as 0), then the outputs
-  size_t slices, qb_ptr, qb_idx, gbar, input_bytes;
+  // input region: slices | qb_ptr | qb_idx, then the outputs
+  size_t slices, qb_ptr, qb_idx, input_bytes;
   size_t row_ptr, sched, nnz_q, nref_q, ref_base_q, pairs_q, totals, col_idx, pairs, ref_ptr,
       kind, ref_idx, total;
   int64_t cap_e, cap_r, n_qb;
@@ -39,11 +38,16 @@ struct BuildLaunch {
   uint8_t *kind;
   int64_t *totals;
   int64_t cap_entries, cap_refs;
-  int32_t *grid_bar;                // zero at launch (part of the uploaded input region)
+  uint32_t off_qb_ptr, off_qb_idx;  // byte offsets of qb_ptr / qb_idx in the input image
+  int32_t *grid_bar, *grid_dep;     // set by build_tiles_launch
   unsigned long long wait_ns;       // bound of the single-launch build's grid barrier
 };
 
-int build_tiles_launch(const BuildLaunch &b, cudaStream_t s);
+// Uploads the input region's host image `img` (slices at offset 0, then
+// qb_ptr, qb_idx) to the start of the workspace `ws` and builds.  Small
+// images ride in the launch's parameters instead (no copy); the build then
+// writes the slices into the workspace itself.
+int build_tiles_launch(BuildLaunch b, const uint8_t *img, size_t img_bytes, void *ws, cudaStream_t s);
 
 int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int hq, int hk, int d,
                float scale, const attn_tiles_t *tiles, void *out, int out_dtype, float *lse,

@@ -33,8 +33,11 @@
 // has many, or split one slice's key tiles when it has few.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
+#include <mutex>
 
 #include "attn_internal.h"
 #include "ptx.cuh"
@@ -42,6 +45,12 @@
 namespace attn {
 
 constexpr int BT = 256;   // threads of the count / fill CTAs
+
+// Where a build reads its inputs: the workspace, or the launch's parameters.
+struct Inputs {
+  const attn_slice_t *slices;
+  const int32_t *qb_ptr, *qb_idx;
+};
 
 __device__ __forceinline__ void row_interval(const attn_slice_t &s, int i, int &lo, int &hi) {
   const int a = i - s.q_start, lq = s.q_end - s.q_start, lk = s.k_end - s.k_start;
@@ -134,7 +143,7 @@ __device__ int block_excl_scan(int v, int *sh, int *total) {
 // (nref) of query tile qt, accumulated in shared memory; the slices are those
 // of the query tile's bucket, and each warp takes one (slice, key tile) pair
 // at a time.
-__device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref) {
+__device__ void count_tile_row(const BuildLaunch &b, const Inputs in, int qt, int *cnt, int *nref) {
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int NW = BT / 32;
@@ -143,7 +152,7 @@ __device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref
     nref[t] = 0;
   }
   __syncthreads();
-  const int u0 = b.qb_ptr[qt], u1 = b.qb_ptr[qt + 1];
+  const int u0 = in.qb_ptr[qt], u1 = in.qb_ptr[qt + 1];
   auto tally = [&](const attn_slice_t &s, int kt) {
     const int c = warp_pairs_fast(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane);
     if (c > 0 && lane == 0) {
@@ -154,7 +163,7 @@ __device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref
   if (u1 - u0 < NW) {
     // few slices: the warps split each slice's key tiles
     for (int u = u0; u < u1; ++u) {
-      const attn_slice_t s = b.slices[b.qb_idx[u]];
+      const attn_slice_t s = in.slices[in.qb_idx[u]];
       int kt0, kt1;
       touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
       for (int kt = kt0 + warp; kt <= kt1; kt += NW) tally(s, kt);
@@ -162,7 +171,7 @@ __device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref
   } else {
     // many slices: one warp per slice
     for (int u = u0 + warp; u < u1; u += NW) {
-      const attn_slice_t s = b.slices[b.qb_idx[u]];
+      const attn_slice_t s = in.slices[in.qb_idx[u]];
       int kt0, kt1;
       touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
       for (int kt = kt0; kt <= kt1; ++kt) tally(s, kt);
@@ -173,8 +182,8 @@ __device__ void count_tile_row(const BuildLaunch &b, int qt, int *cnt, int *nref
 
 // Count phase of query tile qt: per-key-tile counts (cnt, nref, kept in
 // shared memory) -> the tile's entries, references and pairs.
-__device__ void count_phase(const BuildLaunch &b, int qt, int *cnt, int *nref, int *sh) {
-  count_tile_row(b, qt, cnt, nref);
+__device__ void count_phase(const BuildLaunch &b, const Inputs in, int qt, int *cnt, int *nref, int *sh) {
+  count_tile_row(b, in, qt, cnt, nref);
   const int full = b.tq * b.tk;
   int e = 0, r = 0;
   long long pr = 0;
@@ -208,8 +217,8 @@ __device__ void count_phase(const BuildLaunch &b, int qt, int *cnt, int *nref, i
 // ascending key-tile order and its slice references.  `recount` recomputes
 // cnt / nref (two-launch path); the single-launch path still has them.
 // The per-tile counters of other CTAs are read through L2 (__ldcg).
-__device__ void fill_phase(const BuildLaunch &b, int qt, int *cnt, int *nref, int *rpos, int *sh,
-                           bool recount) {
+__device__ void fill_phase(const BuildLaunch &b, const Inputs in, int qt, int *cnt, int *nref, int *rpos,
+                           int *sh, bool recount) {
   const int w = __ldcg(b.nnz_q + qt);
 
   // offsets of this query tile (sums over the preceding ones), and the
@@ -262,7 +271,7 @@ __device__ void fill_phase(const BuildLaunch &b, int qt, int *cnt, int *nref, in
   // capacity exceeded: leave this tile's lists unwritten (the status says so)
   if (row_start + w > b.cap_entries || ref_start + __ldcg(b.nref_q + qt) > b.cap_refs) return;
 
-  if (recount) count_tile_row(b, qt, cnt, nref);
+  if (recount) count_tile_row(b, in, qt, cnt, nref);
   const int full = b.tq * b.tk;
   // entries of this query tile in ascending key-tile order: each thread owns
   // a contiguous run of key tiles so a single scan orders them
@@ -294,14 +303,14 @@ __device__ void fill_phase(const BuildLaunch &b, int qt, int *cnt, int *nref, in
   // bucket in ascending slice id, so each list comes out ordered
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u0 = b.qb_ptr[qt], u1 = b.qb_ptr[qt + 1];
+  const int u0 = in.qb_ptr[qt], u1 = in.qb_ptr[qt + 1];
   for (int kt = warp; kt < b.nk; kt += BT / 32) {
     if (cnt[kt] <= 0 || cnt[kt] == full) continue;
     int pos = rpos[kt];
     const int c0 = kt * b.tk, c1 = min((kt + 1) * b.tk, b.sk);
     for (int u = u0; u < u1; ++u) {
-      const int sid = b.qb_idx[u];
-      const attn_slice_t s = b.slices[sid];
+      const int sid = in.qb_idx[u];
+      const attn_slice_t s = in.slices[sid];
       if (s.k_end <= c0 || s.k_start >= c1) continue;
       if (warp_pairs_fast(s, r0, r1, c0, c1, lane) > 0) {
         if (lane == 0) b.ref_idx[pos] = sid;
@@ -313,28 +322,59 @@ __device__ void fill_phase(const BuildLaunch &b, int qt, int *cnt, int *nref, in
 
 __global__ void __launch_bounds__(BT) count_kernel(const BuildLaunch b) {
   extern __shared__ int shm[];
-  count_phase(b, blockIdx.x, shm, shm + b.nk, shm + 2 * b.nk);
+  count_phase(b, Inputs{b.slices, b.qb_ptr, b.qb_idx}, blockIdx.x, shm, shm + b.nk, shm + 2 * b.nk);
 }
 
 __global__ void __launch_bounds__(BT) fill_kernel(const BuildLaunch b) {
   extern __shared__ int shm[];
-  fill_phase(b, blockIdx.x, shm, shm + b.nk, shm + 2 * b.nk, shm + 3 * b.nk, true);
+  fill_phase(b, Inputs{b.slices, b.qb_ptr, b.qb_idx}, blockIdx.x, shm, shm + b.nk, shm + 2 * b.nk,
+             shm + 3 * b.nk, true);
 }
+
+// Input images of up to kParamImage bytes travel in the single-launch
+// build's parameters.
+constexpr int kParamImage = 2048;
+template <int N>
+struct BuildImage {
+  int32_t w[N / 4];
+};
+
+// Grid barriers of single-launch builds: one (arrived, departed) pair of
+// counters per launch from a ring (host side, round robin); both start at 0
+// (static device memory) and the launch's last CTA to depart puts both back
+// to 0, so no launch needs them cleared first.
+constexpr int kBarSlots = 1024;
+__device__ int g_build_bar[2 * kBarSlots];
 
 // Both phases in one cooperative launch (every CTA resident): the counts
 // stay in shared memory across a grid-wide barrier, so nothing is
-// recounted and one launch is saved.  The barrier counter starts at 0 (it is
-// part of the uploaded input region).  Its wait is bounded: a CTA that gives
-// up records ATTN_ERR_TIMEOUT in the totals' status and poisons the counter,
-// and every CTA that sees the poison (CTA 0 included, which would otherwise
-// write the status) skips the fill.
+// recounted and one launch is saved.  The barrier's wait is bounded: a CTA
+// that gives up records ATTN_ERR_TIMEOUT in the totals' status and poisons
+// the counter, and every CTA that sees the poison (CTA 0 included, which
+// would otherwise write the status) skips the fill.  PARAM: the inputs are
+// read from `img` (the launch's parameters), and CTA 0 also writes the
+// slices into the workspace for the kernels that follow.
 constexpr int kBarrierPoison = 1 << 30;
 
-__global__ void __launch_bounds__(BT) build_kernel(const BuildLaunch b) {
+template <bool PARAM>
+__global__ void __launch_bounds__(BT) build_kernel(const BuildLaunch b,
+                                                   const __grid_constant__ BuildImage<kParamImage> img) {
   extern __shared__ int shm[];
   int *cnt = shm, *nref = shm + b.nk, *rpos = shm + 2 * b.nk, *sh = shm + 3 * b.nk;
   const int qt = blockIdx.x;
-  count_phase(b, qt, cnt, nref, sh);
+  Inputs in{b.slices, b.qb_ptr, b.qb_idx};
+  if (PARAM) {
+    const uint8_t *base = reinterpret_cast<const uint8_t *>(img.w);
+    in.slices = reinterpret_cast<const attn_slice_t *>(base);
+    in.qb_ptr = reinterpret_cast<const int32_t *>(base + b.off_qb_ptr);
+    in.qb_idx = reinterpret_cast<const int32_t *>(base + b.off_qb_idx);
+    if (qt == 0) {
+      int32_t *dst = reinterpret_cast<int32_t *>(const_cast<attn_slice_t *>(b.slices));
+      const int words = static_cast<int>(sizeof(attn_slice_t) / 4) * b.n_slices;
+      for (int i = threadIdx.x; i < words; i += BT) dst[i] = img.w[i];
+    }
+  }
+  count_phase(b, in, qt, cnt, nref, sh);
   __shared__ int arrived;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -353,52 +393,85 @@ __global__ void __launch_bounds__(BT) build_kernel(const BuildLaunch b) {
     }
     __threadfence();
     arrived = v < kBarrierPoison;
+    // the last CTA out resets this launch's barrier slot
+    if (atomicAdd(b.grid_dep, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(b.grid_bar, 0);
+      atomicExch(b.grid_dep, 0);
+    }
   }
   __syncthreads();
   if (!arrived) return;
-  fill_phase(b, qt, cnt, nref, rpos, sh, false);
+  fill_phase(b, in, qt, cnt, nref, rpos, sh, false);
 }
 
-int build_tiles_launch(const BuildLaunch &b, cudaStream_t s) {
+int build_tiles_launch(BuildLaunch b, const uint8_t *img, size_t img_bytes, void *ws, cudaStream_t s) {
   const size_t sm_count = (2 * static_cast<size_t>(b.nk) + 64) * sizeof(int);
   const size_t sm_fill = (3 * static_cast<size_t>(b.nk) + 64) * sizeof(int);
   constexpr int kMaxDev = 64;
-  static int coresident[kMaxDev] = {};   // CTAs of build_kernel that fit at once, per device
+  static int coresident[kMaxDev][2] = {};   // CTAs of build_kernel<PARAM> that fit at once
   static size_t coresident_smem[kMaxDev] = {};
+  static int *bar_base[kMaxDev] = {};
+  static std::atomic<unsigned> bar_seq{0};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
-  static bool configured[kMaxDev] = {};
-  if (!configured[dev]) {
-    if (cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             200 * 1024) != cudaSuccess ||
-        cudaFuncSetAttribute(fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             200 * 1024) != cudaSuccess ||
-        cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             200 * 1024) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    configured[dev] = true;
-  }
-  if (b.nq <= 0) return ATTN_OK;
-  // one launch when every query tile's CTA can be resident at once
-  if (coresident_smem[dev] != sm_fill) {
-    int per_sm = 0, sms = 0, coop = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_kernel, BT, sm_fill) !=
-            cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    coresident[dev] = coop ? per_sm * sms : 0;
-    coresident_smem[dev] = sm_fill;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    static bool configured[kMaxDev] = {};
+    if (!configured[dev]) {
+      void *ptr = nullptr;
+      if (cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               200 * 1024) != cudaSuccess ||
+          cudaFuncSetAttribute(fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               200 * 1024) != cudaSuccess ||
+          cudaFuncSetAttribute(build_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               200 * 1024) != cudaSuccess ||
+          cudaFuncSetAttribute(build_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               200 * 1024) != cudaSuccess ||
+          cudaGetSymbolAddress(&ptr, g_build_bar) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      bar_base[dev] = static_cast<int *>(ptr);
+      configured[dev] = true;
+    }
+    // one launch when every query tile's CTA can be resident at once
+    if (coresident_smem[dev] != sm_fill) {
+      int per_sm[2] = {0, 0}, sms = 0, coop = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[0], build_kernel<false>, BT, sm_fill) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[1], build_kernel<true>, BT, sm_fill) !=
+              cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      coresident[dev][0] = coop ? per_sm[0] * sms : 0;
+      coresident[dev][1] = coop ? per_sm[1] * sms : 0;
+      coresident_smem[dev] = sm_fill;
+    }
   }
   // ATTN_BUILD_TWO_LAUNCH=1 in the environment selects the two-launch path
-  // (used by the tests to check that both paths give the same metadata)
+  // (used by the tests to check that all paths give the same metadata)
   const char *two = std::getenv("ATTN_BUILD_TWO_LAUNCH");
   const bool force_two = two && two[0] == '1';
-  if (!force_two && b.nq <= coresident[dev]) {
-    BuildLaunch arg = b;
-    void *args[] = {&arg};
-    if (cudaLaunchCooperativeKernel(reinterpret_cast<void *>(build_kernel), dim3(b.nq), dim3(BT),
-                                    args, sm_fill, s) != cudaSuccess)
+  const bool param = img_bytes <= static_cast<size_t>(kParamImage) && !force_two &&
+                     b.nq <= coresident[dev][1];
+  if (b.nq <= 0 || !param) {
+    if (img_bytes > 0 && cudaMemcpyAsync(ws, img, img_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (b.nq <= 0) return ATTN_OK;
+  }
+  BuildImage<kParamImage> im;
+  if (param) {
+    std::memset(&im, 0, sizeof(im));
+    std::memcpy(im.w, img, img_bytes);
+  }
+  if (param || (!force_two && b.nq <= coresident[dev][0])) {
+    const unsigned slot = bar_seq.fetch_add(1) % kBarSlots;
+    b.grid_bar = bar_base[dev] + slot;
+    b.grid_dep = bar_base[dev] + kBarSlots + slot;
+    void *args[] = {&b, &im};
+    const void *fn = param ? reinterpret_cast<const void *>(build_kernel<true>)
+                           : reinterpret_cast<const void *>(build_kernel<false>);
+    if (cudaLaunchCooperativeKernel(fn, dim3(b.nq), dim3(BT), args, sm_fill, s) != cudaSuccess)
       return ATTN_ERR_CUDA;
     return ATTN_OK;
   }

@@ -92,8 +92,6 @@ extern "C" int attn_build_tiles_noalloc(const attn_slice_t *h_slices, int n_slic
 
   std::vector<uint8_t> img;
   stage_inputs(h_slices, n_slices, nq, tile_q, L, &img);
-  if (cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return ATTN_ERR_CUDA;
   // The counters are written (not accumulated) by the count kernel before
   // the fill kernel reads them, so the previous call's contents in
   // the shared array need no clearing.
@@ -112,7 +110,8 @@ extern "C" int attn_build_tiles_noalloc(const attn_slice_t *h_slices, int n_slic
   b.nref_q = reinterpret_cast<int32_t *>(sc + 4 * static_cast<size_t>(attn::kMaxQTiles));
   b.ref_base_q = reinterpret_cast<int32_t *>(sc + 8 * static_cast<size_t>(attn::kMaxQTiles));
   b.pairs_q = reinterpret_cast<int64_t *>(sc + 12 * static_cast<size_t>(attn::kMaxQTiles));
-  b.grid_bar = reinterpret_cast<int32_t *>(ws + L.gbar);
+  b.off_qb_ptr = static_cast<uint32_t>(L.qb_ptr);
+  b.off_qb_idx = static_cast<uint32_t>(L.qb_idx);
   b.wait_ns = attn::wait_limit_ns();
   b.row_ptr = t.row_ptr;
   b.col_idx = t.col_idx;
@@ -124,7 +123,7 @@ extern "C" int attn_build_tiles_noalloc(const attn_slice_t *h_slices, int n_slic
   b.totals = t.totals;
   b.cap_entries = L.cap_e;
   b.cap_refs = L.cap_r;
-  if ((rc = attn::build_tiles_launch(b, s)) != ATTN_OK) return rc;
+  if ((rc = attn::build_tiles_launch(b, img.data(), img.size(), ws, s)) != ATTN_OK) return rc;
   *tiles = t;
   return ATTN_OK;
 }
