@@ -94,22 +94,6 @@ __device__ __forceinline__ int warp_pairs_fast(const attn_slice_t &s, int r0, in
   return warp_pairs_in(s, r0, r1, c0, c1, lane);
 }
 
-// Key tiles [*kt0, *kt1] that slice s can touch within rows [r0, r1); empty
-// when *kt1 < *kt0.
-__device__ __forceinline__ void touched_ktiles(const attn_slice_t &s, int r0, int r1, int tk,
-                                               int *kt0, int *kt1) {
-  const int a = max(r0, s.q_start), b = min(r1, s.q_end);
-  int lo, hi, lo2, hi2;
-  row_interval(s, a, lo, hi);
-  row_interval(s, b - 1, lo2, hi2);
-  if (hi2 <= lo) {
-    *kt0 = 1;
-    *kt1 = 0;
-    return;
-  }
-  *kt0 = lo / tk;
-  *kt1 = (hi2 - 1) / tk;
-}
 
 // Block-wide exclusive scan of one int per thread (BT threads); returns the
 // prefix and writes the block total to *total.
@@ -139,43 +123,114 @@ __device__ int block_excl_scan(int v, int *sh, int *total) {
   return before;
 }
 
+// A query tile's bucket is staged in shared memory kChunk slices at a time
+// (one load per thread, all in flight together).
+constexpr int kChunk = BT;
+constexpr int kCutList = 1024;
+__shared__ attn_slice_t s_stage[kChunk];   // staged slices
+__shared__ int s_stage_id[kChunk];          // their ids (reference pass)
+__shared__ int s_stage_off[kChunk];         // their first work item (count pass)
+__shared__ int s_stage_kt0[kChunk];         // their first key tile (count pass)
+
+// Key tiles [*kt0, *kt1] that slice s can touch within rows [r0, r1); empty
+// when *kt1 < *kt0.
+__device__ __forceinline__ void slice_ktiles(const attn_slice_t &s, int r0, int r1, int tk, int *kt0,
+                                             int *kt1) {
+  const int a = max(r0, s.q_start), e = min(r1, s.q_end);
+  *kt0 = 1;
+  *kt1 = 0;
+  if (a >= e) return;
+  int lo_a, hi_a, lo_e, hi_e;
+  row_interval(s, a, lo_a, hi_a);
+  row_interval(s, e - 1, lo_e, hi_e);
+  if (hi_e <= lo_a) return;
+  *kt0 = lo_a / tk;
+  *kt1 = (hi_e - 1) / tk;
+}
+
 // Per-key-tile valid-pair counts (cnt) and numbers of contributing slices
-// (nref) of query tile qt, accumulated in shared memory; the slices are those
-// of the query tile's bucket, and each warp takes one (slice, key tile) pair
-// at a time.
-__device__ void count_tile_row(const BuildLaunch &b, const Inputs in, int qt, int *cnt, int *nref) {
+// (nref) of query tile qt, in shared memory; the slices are those of the
+// query tile's bucket.  Per staged chunk, every (slice, key tile it can
+// touch) pair is one work item, spread over the threads by a block scan.
+// A tile that every row's interval covers counts rows x width at once, a
+// tile no row reaches is skipped, and a tile cut by an interval end goes to
+// a shared list, whose tiles the warps then count row by row,
+// lane-parallel (a full list makes the thread count the tile itself).
+__device__ void count_tile_row(const BuildLaunch &b, const Inputs in, int qt, int *cnt, int *nref, int *sh) {
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int NW = BT / 32;
-  for (int t = threadIdx.x; t < b.nk; t += BT) {
+  const int tid = static_cast<int>(threadIdx.x), warp = tid >> 5, lane = tid & 31;
+  __shared__ int cut_n;
+  __shared__ int2 cut[kCutList];   // (staged slice, key tile)
+  for (int t = tid; t < b.nk; t += BT) {
     cnt[t] = 0;
     nref[t] = 0;
   }
-  __syncthreads();
   const int u0 = in.qb_ptr[qt], u1 = in.qb_ptr[qt + 1];
-  auto tally = [&](const attn_slice_t &s, int kt) {
-    const int c = warp_pairs_fast(s, r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane);
-    if (c > 0 && lane == 0) {
-      atomicAdd(&cnt[kt], c);
-      atomicAdd(&nref[kt], 1);
-    }
-  };
-  if (u1 - u0 < NW) {
-    // few slices: the warps split each slice's key tiles
-    for (int u = u0; u < u1; ++u) {
-      const attn_slice_t s = in.slices[in.qb_idx[u]];
+  for (int base = u0; base < u1; base += kChunk) {
+    const int m = min(kChunk, u1 - base);
+    int ntiles = 0;
+    if (tid < m) {
+      const attn_slice_t s = in.slices[in.qb_idx[base + tid]];
       int kt0, kt1;
-      touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
-      for (int kt = kt0 + warp; kt <= kt1; kt += NW) tally(s, kt);
+      slice_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
+      s_stage[tid] = s;
+      s_stage_kt0[tid] = kt0;
+      ntiles = max(0, kt1 - kt0 + 1);
     }
-  } else {
-    // many slices: one warp per slice
-    for (int u = u0 + warp; u < u1; u += NW) {
-      const attn_slice_t s = in.slices[in.qb_idx[u]];
-      int kt0, kt1;
-      touched_ktiles(s, r0, r1, b.tk, &kt0, &kt1);
-      for (int kt = kt0; kt <= kt1; ++kt) tally(s, kt);
+    if (tid == 0) cut_n = 0;
+    int total;
+    const int off = block_excl_scan(ntiles, sh, &total);   // synchronises the block
+    if (tid < m) s_stage_off[tid] = off;
+    __syncthreads();
+    for (int wi = tid; wi < total; wi += BT) {
+      // the item's slice: the last staged one whose first item is <= wi
+      int lo = 0, hi = m - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_stage_off[mid] <= wi) lo = mid;
+        else hi = mid - 1;
+      }
+      const attn_slice_t &s = s_stage[lo];
+      const int kt = s_stage_kt0[lo] + (wi - s_stage_off[lo]);
+      const int c0 = kt * b.tk, c1 = min(c0 + b.tk, b.sk);
+      const int a = max(r0, s.q_start), e = min(r1, s.q_end);
+      int lo_a, hi_a, lo_e, hi_e;
+      row_interval(s, a, lo_a, hi_a);
+      row_interval(s, e - 1, lo_e, hi_e);
+      if (hi_e <= c0 || lo_a >= c1) continue;
+      if (lo_e <= c0 && hi_a >= c1) {
+        atomicAdd(&cnt[kt], (e - a) * (c1 - c0));
+        atomicAdd(&nref[kt], 1);
+        continue;
+      }
+      const int k = atomicAdd(&cut_n, 1);
+      if (k < kCutList) {
+        cut[k] = make_int2(lo, kt);
+      } else {
+        int c = 0;
+        for (int i = a; i < e; ++i) {
+          int l, h;
+          row_interval(s, i, l, h);
+          c += max(0, min(h, c1) - max(l, c0));
+        }
+        if (c > 0) {
+          atomicAdd(&cnt[kt], c);
+          atomicAdd(&nref[kt], 1);
+        }
+      }
     }
+    __syncthreads();
+    const int n_cut = min(cut_n, kCutList);
+    for (int k = warp; k < n_cut; k += BT / 32) {
+      const int2 item = cut[k];
+      const int kt = item.y;
+      const int c = warp_pairs_in(s_stage[item.x], r0, r1, kt * b.tk, min((kt + 1) * b.tk, b.sk), lane);
+      if (c > 0 && lane == 0) {
+        atomicAdd(&cnt[kt], c);
+        atomicAdd(&nref[kt], 1);
+      }
+    }
+    __syncthreads();
   }
   __syncthreads();
 }
@@ -183,7 +238,7 @@ __device__ void count_tile_row(const BuildLaunch &b, const Inputs in, int qt, in
 // Count phase of query tile qt: per-key-tile counts (cnt, nref, kept in
 // shared memory) -> the tile's entries, references and pairs.
 __device__ void count_phase(const BuildLaunch &b, const Inputs in, int qt, int *cnt, int *nref, int *sh) {
-  count_tile_row(b, in, qt, cnt, nref);
+  count_tile_row(b, in, qt, cnt, nref, sh);
   const int full = b.tq * b.tk;
   int e = 0, r = 0;
   long long pr = 0;
@@ -271,7 +326,7 @@ __device__ void fill_phase(const BuildLaunch &b, const Inputs in, int qt, int *c
   // capacity exceeded: leave this tile's lists unwritten (the status says so)
   if (row_start + w > b.cap_entries || ref_start + __ldcg(b.nref_q + qt) > b.cap_refs) return;
 
-  if (recount) count_tile_row(b, in, qt, cnt, nref);
+  if (recount) count_tile_row(b, in, qt, cnt, nref, sh);
   const int full = b.tq * b.tk;
   // entries of this query tile in ascending key-tile order: each thread owns
   // a contiguous run of key tiles so a single scan orders them
@@ -298,25 +353,43 @@ __device__ void fill_phase(const BuildLaunch &b, const Inputs in, int qt, int *c
     ++ebase;
     if (masked) rbase += nref[t];
   }
+  // slice references of MASKED tiles: the threads list them (nref is free
+  // now), then one warp per listed tile walks the bucket in ascending slice
+  // id, so each tile's references come out ordered
+  __shared__ int n_masked;
+  if (threadIdx.x == 0) n_masked = 0;
   __syncthreads();
-  // slice references of MASKED tiles: one warp per key tile walks the
-  // bucket in ascending slice id, so each list comes out ordered
+  int *mlist = nref;
+  for (int t = t0; t < t1; ++t)
+    if (cnt[t] > 0 && cnt[t] != full) mlist[atomicAdd(&n_masked, 1)] = t;
+  __syncthreads();
   const int r0 = qt * b.tq, r1 = min(r0 + b.tq, b.sq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u0 = in.qb_ptr[qt], u1 = in.qb_ptr[qt + 1];
-  for (int kt = warp; kt < b.nk; kt += BT / 32) {
-    if (cnt[kt] <= 0 || cnt[kt] == full) continue;
-    int pos = rpos[kt];
-    const int c0 = kt * b.tk, c1 = min((kt + 1) * b.tk, b.sk);
-    for (int u = u0; u < u1; ++u) {
-      const int sid = in.qb_idx[u];
-      const attn_slice_t s = in.slices[sid];
-      if (s.k_end <= c0 || s.k_start >= c1) continue;
-      if (warp_pairs_fast(s, r0, r1, c0, c1, lane) > 0) {
-        if (lane == 0) b.ref_idx[pos] = sid;
-        ++pos;
-      }
+  for (int base = u0; base < u1; base += kChunk) {
+    const int m = min(kChunk, u1 - base);
+    if (static_cast<int>(threadIdx.x) < m) {
+      const int sid = in.qb_idx[base + threadIdx.x];
+      s_stage_id[threadIdx.x] = sid;
+      s_stage[threadIdx.x] = in.slices[sid];
     }
+    __syncthreads();
+    for (int k = warp; k < n_masked; k += BT / 32) {
+      const int kt = mlist[k];
+      int pos = rpos[kt];
+      const int c0 = kt * b.tk, c1 = min((kt + 1) * b.tk, b.sk);
+      for (int i = 0; i < m; ++i) {
+        const attn_slice_t &s = s_stage[i];
+        if (s.k_end <= c0 || s.k_start >= c1) continue;
+        if (warp_pairs_fast(s, r0, r1, c0, c1, lane) > 0) {
+          if (lane == 0) b.ref_idx[pos] = s_stage_id[i];
+          ++pos;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) rpos[kt] = pos;   // the next chunk continues from here
+    }
+    __syncthreads();
   }
 }
 
