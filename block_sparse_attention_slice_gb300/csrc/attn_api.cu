@@ -34,21 +34,31 @@ int check_slices(const attn_slice_t *s, int n, int sq, int sk) {
 // next run.  Lists that come sorted (block grids, most slice lists) skip the
 // sort, and a grid is checked in linear time.
 int check_overlap(const attn_slice_t *s, int n) {
-  std::vector<int> idx;
-  idx.reserve(n);
-  for (int i = 0; i < n; ++i)
-    if (s[i].q_end > s[i].q_start && s[i].k_end > s[i].k_start) idx.push_back(i);
+  // order of the non-empty slices by (q_start, k_start): their own order when
+  // it already is sorted, else a sorted index list (per-thread buffers, kept
+  // across calls)
+  static thread_local std::vector<int> idx, run_end;
+  auto empty = [&](int i) { return s[i].q_end <= s[i].q_start || s[i].k_end <= s[i].k_start; };
   auto before = [&](int a, int b) {
     return s[a].q_start != s[b].q_start ? s[a].q_start < s[b].q_start : s[a].k_start < s[b].k_start;
   };
-  if (!std::is_sorted(idx.begin(), idx.end(), before)) std::sort(idx.begin(), idx.end(), before);
-  const size_t m = idx.size();
-  std::vector<size_t> run_end(m);
-  for (size_t u = m; u-- > 0;)
+  idx.clear();
+  bool sorted = true;
+  int last = -1;
+  for (int i = 0; i < n; ++i) {
+    if (empty(i)) continue;
+    if (last >= 0 && before(i, last)) sorted = false;
+    idx.push_back(i);
+    last = i;
+  }
+  if (!sorted) std::sort(idx.begin(), idx.end(), before);
+  const int m = static_cast<int>(idx.size());
+  run_end.resize(m);
+  for (int u = m; u-- > 0;)
     run_end[u] = (u + 1 < m && s[idx[u + 1]].q_start == s[idx[u]].q_start) ? run_end[u + 1] : u + 1;
-  for (size_t u = 0; u < m; ++u) {
+  for (int u = 0; u < m; ++u) {
     const attn_slice_t &a = s[idx[u]];
-    size_t v = u + 1;
+    int v = u + 1;
     while (v < m && s[idx[v]].q_start < a.q_end) {
       const attn_slice_t &b = s[idx[v]];
       if (b.q_start == a.q_start && b.k_start >= a.k_end) {
@@ -61,6 +71,17 @@ int check_overlap(const attn_slice_t *s, int n) {
   }
   return ATTN_OK;
 }
+
+// x / d for x >= 0, by a shift when d is a power of two
+struct TileDiv {
+  int d, sh = -1;
+  explicit TileDiv(int d_) : d(d_) {
+    if (d_ > 0 && (d_ & (d_ - 1)) == 0)
+      for (sh = 0; (1 << sh) < d_; ++sh) {
+      }
+  }
+  int operator()(int x) const { return sh >= 0 ? x >> sh : x / d; }
+};
 
 int shape_ok(int sq, int sk, int tq, int tk, int *nq, int *nk) {
   if (sq < 1 || sk < 1 || tq < 1 || tk < 1) return ATTN_ERR_INVALID_ARG;
@@ -75,10 +96,11 @@ int shape_ok(int sq, int sk, int tq, int tk, int *nq, int *nk) {
 WsLayout layout(const attn_slice_t *s, int n, int nq, int nk, int tq, int tk) {
   WsLayout L{};
   int64_t touched = 0, touched_q = 0;
+  const TileDiv dq(tq), dk(tk);
   for (int i = 0; i < n; ++i) {
     if (s[i].q_end <= s[i].q_start || s[i].k_end <= s[i].k_start) continue;
-    const int64_t a = (s[i].q_end - 1) / tq - s[i].q_start / tq + 1;
-    const int64_t b = (s[i].k_end - 1) / tk - s[i].k_start / tk + 1;
+    const int64_t a = dq(s[i].q_end - 1) - dq(s[i].q_start) + 1;
+    const int64_t b = dk(s[i].k_end - 1) - dk(s[i].k_start) + 1;
     touched += a * b;
     touched_q += a;
   }
@@ -114,19 +136,24 @@ WsLayout layout(const attn_slice_t *s, int n, int nq, int nk, int tq, int tk) {
 
 void stage_inputs(const attn_slice_t *s, int n, int nq, int tq, const WsLayout &L,
                   std::vector<uint8_t> *img) {
-  img->assign(L.input_bytes, 0);
+  // every byte is written below: the slices and the bucket ids fully, the
+  // bucket pointers after zeroing, so the buffer is not cleared first
+  img->resize(L.input_bytes);
   if (n > 0) std::memcpy(img->data() + L.slices, s, sizeof(attn_slice_t) * n);
   int32_t *ptr = reinterpret_cast<int32_t *>(img->data() + L.qb_ptr);
   int32_t *idx = reinterpret_cast<int32_t *>(img->data() + L.qb_idx);
+  std::memset(ptr, 0, sizeof(int32_t) * (nq + 1));
+  const TileDiv dq(tq);
   for (int i = 0; i < n; ++i) {
     if (s[i].q_end <= s[i].q_start || s[i].k_end <= s[i].k_start) continue;
-    for (int q = s[i].q_start / tq; q <= (s[i].q_end - 1) / tq; ++q) ++ptr[q + 1];
+    for (int q = dq(s[i].q_start), q1 = dq(s[i].q_end - 1); q <= q1; ++q) ++ptr[q + 1];
   }
   for (int q = 0; q < nq; ++q) ptr[q + 1] += ptr[q];
-  std::vector<int32_t> fill(ptr, ptr + nq);
+  static thread_local std::vector<int32_t> fill;
+  fill.assign(ptr, ptr + nq);
   for (int i = 0; i < n; ++i) {          // ascending ids within every bucket
     if (s[i].q_end <= s[i].q_start || s[i].k_end <= s[i].k_start) continue;
-    for (int q = s[i].q_start / tq; q <= (s[i].q_end - 1) / tq; ++q) idx[fill[q]++] = i;
+    for (int q = dq(s[i].q_start), q1 = dq(s[i].q_end - 1); q <= q1; ++q) idx[fill[q]++] = i;
   }
 }
 
@@ -186,7 +213,7 @@ int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
   t.slices = reinterpret_cast<attn_slice_t *>(ws + L.slices);
   t.scratch = reinterpret_cast<int32_t *>(ws + L.nnz_q);
 
-  std::vector<uint8_t> img;
+  static thread_local std::vector<uint8_t> img;   // kept across calls
   stage_inputs(h_slices, n_slices, nq, tile_q, L, &img);
   attn::BuildLaunch b;
   b.slices = t.slices;

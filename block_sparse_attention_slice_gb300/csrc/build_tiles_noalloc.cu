@@ -90,7 +90,7 @@ extern "C" int attn_build_tiles_noalloc(const attn_slice_t *h_slices, int n_slic
   t.slices = reinterpret_cast<attn_slice_t *>(ws + L.slices);
   t.scratch = reinterpret_cast<int32_t *>(sc);
 
-  std::vector<uint8_t> img;
+  static thread_local std::vector<uint8_t> img;   // kept across calls
   stage_inputs(h_slices, n_slices, nq, tile_q, L, &img);
   // The counters are written (not accumulated) by the count kernel before
   // the fill kernel reads them, so the previous call's contents in
