@@ -123,10 +123,8 @@ def _slice_array(slices) -> ctypes.Array:
 def host_slices(slices):
     """Slice list as a contiguous int32 [n, 5] host array plus its count.
 
-    Pageable memory on purpose: the upload inside attn_build_tiles stages a
-    pageable source before it returns, so the caller may reuse or free the
-    array right away (a page-locked source would be read later, when the
-    stream reaches the copy)."""
+    attn_build_tiles copies the slices into an input image of its own before
+    it returns, so the caller may reuse or free the array right away."""
     a = np.ascontiguousarray(np.asarray(slices, dtype=np.int32).reshape(-1, 5))
     return (a if len(a) else np.zeros((1, 5), np.int32)), len(a)
 

@@ -130,12 +130,14 @@ int attn_tiles_workspace_bytes(const attn_slice_t *h_slices, int n_slices, int s
  *   tile_q/k   tile shape, 1..1024 each; ceil(sk / tile_k) <= 8192
  *   d_ws       device workspace of ws_bytes >= attn_tiles_workspace_bytes()
  *   tiles      host struct, filled with the shape and device pointers
- * The slice list is read on the host during the call and its upload is
- * enqueued on `stream` (cudaMemcpyAsync): a pageable h_slices is staged
- * before the call returns and may be reused at once; a page-locked one must
- * stay unchanged until the stream has executed the copy.  The metadata is
- * produced by three kernels on `stream`.  The counts are exact integers, so
- * the result is bit-identical run to run.  Errors: INVALID_ARG, OVERLAP,
+ * The slice list is read on the host during the call.  The call copies it,
+ * with the per-query-tile slice lists it derives, into an input image of its
+ * own, so h_slices may be reused or freed as soon as the call returns.  Up to
+ * 2 KB, the image travels in the build kernel's launch parameters; a larger
+ * one is copied to the start of d_ws (cudaMemcpyAsync on `stream`).  The
+ * metadata is produced on `stream` by one cooperative kernel when every query
+ * tile's CTA fits on the GPU at once, else by two kernels.  The counts are
+ * exact integers, so the result is bit-identical run to run.  Errors: INVALID_ARG, OVERLAP,
  * UNSUPPORTED (tile or grid too large), CAPACITY (ws_bytes too small), CUDA. */
 int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
                      int tile_q, int tile_k, void *d_ws, size_t ws_bytes,
