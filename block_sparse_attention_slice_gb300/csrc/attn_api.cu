@@ -293,10 +293,17 @@ int attn_fwd(const void *q, const void *k, const void *v, int sq, int sk, int hq
   if (tiles->tile_q != ATTN_FWD_TILE_Q || tiles->tile_k != ATTN_FWD_TILE_K)
     return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_UNSUPPORTED;
-  const char *qb = static_cast<const char *>(q), *ob = static_cast<const char *>(out);
-  const size_t qbytes = static_cast<size_t>(sq) * hq * d * 2;
+  // q, k, v (read through TMA while O is written) must not overlap out
+  const char *ob = static_cast<const char *>(out);
   const size_t obytes = static_cast<size_t>(sq) * hq * d * (out_dtype == ATTN_DTYPE_F32 ? 4 : 2);
-  if (qb < ob + obytes && ob < qb + qbytes) return ATTN_ERR_INVALID_ARG;   // q aliases out
+  const size_t qbytes = static_cast<size_t>(sq) * hq * d * 2;
+  const size_t kvbytes = static_cast<size_t>(sk) * hk * d * 2;
+  auto meets_out = [&](const void *x, size_t n) {
+    const char *xb = static_cast<const char *>(x);
+    return xb < ob + obytes && ob < xb + n;
+  };
+  if (meets_out(q, qbytes) || meets_out(k, kvbytes) || meets_out(v, kvbytes))
+    return ATTN_ERR_INVALID_ARG;
   return attn::fwd_launch(q, k, v, sq, sk, hq, hk, d, scale, tiles, out, out_dtype, lse,
                           reinterpret_cast<cudaStream_t>(stream));
 }
@@ -354,10 +361,13 @@ int attn_merge(const void *const *h_o_parts, const float *const *h_lse_parts, in
 int attn_last_device_error(attn_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  unsigned int st = 0, sb = 0;
-  if (attn::fwd_status_take(&st) != ATTN_OK || attn::bwd_status_take(&sb) != ATTN_OK)
+  unsigned int st[3] = {0, 0, 0};
+  if (attn::build_status_take(&st[0]) != ATTN_OK || attn::fwd_status_take(&st[1]) != ATTN_OK ||
+      attn::bwd_status_take(&st[2]) != ATTN_OK)
     return ATTN_ERR_CUDA;
-  return (st || sb) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+  for (unsigned int x : st)
+    if (x) return static_cast<int>(x);
+  return ATTN_OK;
 }
 
 int attn_set_wait_limit_ns(int64_t ns) {

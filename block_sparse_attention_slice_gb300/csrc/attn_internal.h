@@ -39,7 +39,7 @@ struct BuildLaunch {
   int64_t *totals;
   int64_t cap_entries, cap_refs;
   uint32_t off_qb_ptr, off_qb_idx;  // byte offsets of qb_ptr / qb_idx in the input image
-  int32_t *grid_bar, *grid_dep;     // set by build_tiles_launch
+  int32_t *grid_bar, *grid_dep, *grid_state;   // set by build_tiles_launch
   unsigned long long wait_ns;       // bound of the single-launch build's grid barrier
 };
 
@@ -48,6 +48,9 @@ struct BuildLaunch {
 // images ride in the launch's parameters instead (no copy); the build then
 // writes the slices into the workspace itself.
 int build_tiles_launch(BuildLaunch b, const uint8_t *img, size_t img_bytes, void *ws, cudaStream_t s);
+// Reads and clears the first failure status of single-launch builds on the
+// current device (0 when none).
+int build_status_take(unsigned int *status);
 
 int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int hq, int hk, int d,
                float scale, const attn_tiles_t *tiles, void *out, int out_dtype, float *lse,

@@ -412,22 +412,30 @@ struct BuildImage {
   int32_t w[N / 4];
 };
 
-// Grid barriers of single-launch builds: one (arrived, departed) pair of
-// counters per launch from a ring (host side, round robin); both start at 0
-// (static device memory) and the launch's last CTA to depart puts both back
-// to 0, so no launch needs them cleared first.
+// Grid barriers of single-launch builds: one (arrived, departed, decision)
+// triple of words per launch from a ring (host side, round robin); all start
+// at 0 (static device memory) and the launch's last CTA to depart puts them
+// back to 0, so no launch needs them cleared first.
 constexpr int kBarSlots = 1024;
-__device__ int g_build_bar[2 * kBarSlots];
+__device__ int g_build_bar[3 * kBarSlots];
+constexpr int kBarGo = 1, kBarAbort = 2;   // decision word: 0 while undecided
+
+// First failure status of a single-launch build on this device (its bounded
+// grid barrier ran out); read and cleared by attn_last_device_error().
+__device__ unsigned int g_build_status;
 
 // Both phases in one cooperative launch (every CTA resident): the counts
 // stay in shared memory across a grid-wide barrier, so nothing is
-// recounted and one launch is saved.  The barrier's wait is bounded: a CTA
-// that gives up records ATTN_ERR_TIMEOUT in the totals' status and poisons
-// the counter, and every CTA that sees the poison (CTA 0 included, which
-// would otherwise write the status) skips the fill.  PARAM: the inputs are
-// read from `img` (the launch's parameters), and CTA 0 also writes the
-// slices into the workspace for the kernels that follow.
-constexpr int kBarrierPoison = 1 << 30;
+// recounted and one launch is saved.  The barrier's wait is bounded.  The
+// barrier ends with one decision that every CTA follows: "go", set by the
+// last CTA to arrive, or "abort", set by a CTA whose wait ran out first
+// (only the first of the two compare-and-swaps on the decision word takes).
+// On abort no CTA fills; each writes an empty list for its query tile and
+// CTA 0 writes zero totals with ATTN_ERR_TIMEOUT as the status, so the
+// metadata stays valid (every list empty) and the kernels that read it see
+// the status and refuse it.  PARAM: the inputs are read from `img` (the
+// launch's parameters), and CTA 0 also writes the slices into the workspace
+// for the kernels that follow.
 
 template <bool PARAM>
 __global__ void __launch_bounds__(BT) build_kernel(const BuildLaunch b,
@@ -448,32 +456,49 @@ __global__ void __launch_bounds__(BT) build_kernel(const BuildLaunch b,
     }
   }
   count_phase(b, in, qt, cnt, nref, sh);
-  __shared__ int arrived;
+  __shared__ int go;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();                   // this tile's counters before the arrival
-    atomicAdd(b.grid_bar, 1);
+    if (atomicAdd(b.grid_bar, 1) == static_cast<int>(gridDim.x) - 1) {
+      __threadfence();                 // every arrival (and its counters) before "go"
+      atomicCAS(b.grid_state, 0, kBarGo);
+    }
     const unsigned long long deadline = globaltimer_ns() + b.wait_ns;
-    int v;
-    while ((v = *reinterpret_cast<volatile int *>(b.grid_bar)) < static_cast<int>(gridDim.x)) {
+    int st;
+    while ((st = *reinterpret_cast<volatile int *>(b.grid_state)) == 0) {
       if (globaltimer_ns() > deadline) {
-        atomicAdd(b.grid_bar, kBarrierPoison);
-        atomicExch(reinterpret_cast<unsigned long long *>(b.totals + 3),
-                   static_cast<unsigned long long>(ATTN_ERR_TIMEOUT));
-        v = kBarrierPoison;
+        const int prev = atomicCAS(b.grid_state, 0, kBarAbort);
+        st = prev == 0 ? kBarAbort : prev;
         break;
       }
     }
     __threadfence();
-    arrived = v < kBarrierPoison;
-    // the last CTA out resets this launch's barrier slot
+    go = st == kBarGo;
+    // the last CTA out (every CTA has read the decision) resets the slot
     if (atomicAdd(b.grid_dep, 1) == static_cast<int>(gridDim.x) - 1) {
       atomicExch(b.grid_bar, 0);
+      atomicExch(b.grid_state, 0);
       atomicExch(b.grid_dep, 0);
     }
   }
   __syncthreads();
-  if (!arrived) return;
+  if (!go) {
+    if (threadIdx.x == 0) {
+      b.row_ptr[qt] = 0;
+      b.sched[qt] = qt;
+      if (qt == 0) {
+        b.row_ptr[b.nq] = 0;
+        b.ref_ptr[0] = 0;
+        b.totals[0] = 0;
+        b.totals[1] = 0;
+        b.totals[2] = 0;
+        b.totals[3] = ATTN_ERR_TIMEOUT;
+        atomicCAS(&g_build_status, 0u, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
+      }
+    }
+    return;
+  }
   fill_phase(b, in, qt, cnt, nref, rpos, sh, false);
 }
 
@@ -484,6 +509,7 @@ int build_tiles_launch(BuildLaunch b, const uint8_t *img, size_t img_bytes, void
   static int coresident[kMaxDev][2] = {};   // CTAs of build_kernel<PARAM> that fit at once
   static size_t coresident_smem[kMaxDev] = {};
   static int *bar_base[kMaxDev] = {};
+  int fit[2] = {0, 0};   // this call's copy of coresident[dev], taken under the lock
   static std::atomic<unsigned> bar_seq{0};
   static std::mutex mu;
   int dev = 0;
@@ -520,13 +546,15 @@ int build_tiles_launch(BuildLaunch b, const uint8_t *img, size_t img_bytes, void
       coresident[dev][1] = coop ? per_sm[1] * sms : 0;
       coresident_smem[dev] = sm_fill;
     }
+    fit[0] = coresident[dev][0];
+    fit[1] = coresident[dev][1];
   }
   // ATTN_BUILD_TWO_LAUNCH=1 in the environment selects the two-launch path
   // (used by the tests to check that all paths give the same metadata)
   const char *two = std::getenv("ATTN_BUILD_TWO_LAUNCH");
   const bool force_two = two && two[0] == '1';
   const bool param = img_bytes <= static_cast<size_t>(kParamImage) && !force_two &&
-                     b.nq <= coresident[dev][1];
+                     b.nq <= fit[1];
   if (b.nq <= 0 || !param) {
     if (img_bytes > 0 && cudaMemcpyAsync(ws, img, img_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
       return ATTN_ERR_CUDA;
@@ -537,10 +565,11 @@ int build_tiles_launch(BuildLaunch b, const uint8_t *img, size_t img_bytes, void
     std::memset(&im, 0, sizeof(im));
     std::memcpy(im.w, img, img_bytes);
   }
-  if (param || (!force_two && b.nq <= coresident[dev][0])) {
+  if (param || (!force_two && b.nq <= fit[0])) {
     const unsigned slot = bar_seq.fetch_add(1) % kBarSlots;
     b.grid_bar = bar_base[dev] + slot;
     b.grid_dep = bar_base[dev] + kBarSlots + slot;
+    b.grid_state = bar_base[dev] + 2 * kBarSlots + slot;
     void *args[] = {&b, &im};
     const void *fn = param ? reinterpret_cast<const void *>(build_kernel<true>)
                            : reinterpret_cast<const void *>(build_kernel<false>);
@@ -551,6 +580,15 @@ int build_tiles_launch(BuildLaunch b, const uint8_t *img, size_t img_bytes, void
   count_kernel<<<b.nq, BT, sm_count, s>>>(b);
   fill_kernel<<<b.nq, BT, sm_fill, s>>>(b);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int build_status_take(unsigned int *status) {
+  unsigned int zero = 0;
+  if (cudaMemcpyFromSymbol(status, g_build_status, sizeof(unsigned int)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (*status && cudaMemcpyToSymbol(g_build_status, &zero, sizeof(unsigned int)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
 }
 
 }  // namespace attn

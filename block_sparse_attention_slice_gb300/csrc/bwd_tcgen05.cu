@@ -28,6 +28,9 @@
 
 namespace attn {
 
+// First failure status of backward launches on this device (0 = none): a
+// bounded wait that ran out, or metadata whose build did not finish with
+// ATTN_OK.  Read and cleared by attn_last_device_error().
 __device__ unsigned int g_bwd_status;
 
 constexpr int B_THREADS = 192;     // warps 0-3 element-wise, 4 producer, 5 MMA issuer
@@ -45,7 +48,19 @@ struct BwdParams {
   int grad_f32;
   float scale, scale_log2;
   unsigned long long wait_ns;
+  const long long *meta_status;   // the metadata build's status word (totals[3])
 };
+
+// True when the metadata's build did not finish with ATTN_OK: the kernel
+// then reads none of it and returns at once (uniformly for the whole CTA,
+// before any barrier or tensor memory is set up); the first CTA records the
+// status.
+__device__ __forceinline__ bool meta_refused(const BwdParams &p) {
+  const long long st = *p.meta_status;
+  if (st == ATTN_OK) return false;
+  if (blockIdx.x == 0 && threadIdx.x == 0) atomicCAS(&g_bwd_status, 0u, static_cast<unsigned>(st));
+  return true;
+}
 
 // ------------------------------------------------------------------ D = rowsum(dO * O)
 // One thread per 8 consecutive elements (one 16-byte load of dO, one or two
@@ -117,6 +132,7 @@ __device__ long long block_sum_ll(long long v, long long *red) {
 }
 
 __global__ void __launch_bounds__(256) csc_count_kernel(BwdParams p, int32_t *colcnt) {
+  if (meta_refused(p)) return;
   __shared__ long long red[8];
   const int kt = blockIdx.x;
   long long c = 0;
@@ -128,6 +144,7 @@ __global__ void __launch_bounds__(256) csc_count_kernel(BwdParams p, int32_t *co
 __global__ void __launch_bounds__(256) csc_fill_kernel(BwdParams p, const int32_t *colcnt,
                                                        int32_t *col_ptr, int32_t *col_q,
                                                        int32_t *col_e, int32_t *col_sched) {
+  if (meta_refused(p)) return;
   __shared__ long long red[8];
   __shared__ int scan[256];
   const int kt = blockIdx.x, me = colcnt[kt];
@@ -262,6 +279,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
+  if (meta_refused(p)) return;
   using L = KVLayout<D>;
   using BL = BLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -468,7 +486,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, 512);
-  if (threadIdx.x == 0 && *abort) atomicExch(&g_bwd_status, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
+  if (threadIdx.x == 0 && *abort) atomicCAS(&g_bwd_status, 0u, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
 }
 
 // ------------------------------------------------------------------ dQ per query tile
@@ -544,6 +562,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                  const BwdParams p) {
+  if (meta_refused(p)) return;
   using L = QLayout<D, NS>;
   using BL = BLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -771,7 +790,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, 512);
-  if (threadIdx.x == 0 && *abort) atomicExch(&g_bwd_status, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
+  if (threadIdx.x == 0 && *abort) atomicCAS(&g_bwd_status, 0u, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
 }
 
 // ------------------------------------------------------------------ host side
@@ -849,6 +868,7 @@ int bwd_launch(const void *q, const void *k, const void *v, const void *out, int
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_ns = wait_limit_ns();
+  p.meta_status = reinterpret_cast<const long long *>(tiles->totals + 3);
 
   const long long dthreads = static_cast<long long>(sq) * hq * (d / 8);
   const unsigned dgrid = static_cast<unsigned>((dthreads + 255) / 256);

@@ -54,6 +54,10 @@
 
 namespace attn {
 
+// First failure status of forward launches on this device (0 = none): a
+// bounded wait that ran out (ATTN_ERR_TIMEOUT), or metadata whose build did
+// not finish with ATTN_OK (its status code).  Read and cleared by
+// attn_last_device_error().
 __device__ unsigned int g_fwd_status;
 
 constexpr int BM = 128;           // rows per MMA tile
@@ -82,6 +86,7 @@ struct FwdParams {
   float scale_log2;               // scale * log2(e)
   unsigned long long wait_ns;
   unsigned int *counter;          // this launch's work counter (0 at launch, reset by its last CTA)
+  const long long *meta_status;   // the metadata build's status word (totals[3])
 };
 
 // One resolved tile entry: key tile, kind, reference range and up to two
@@ -149,6 +154,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sb + L::BAR_OFF + 8u * i; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
+  volatile int *meta_bad = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 8);
   Rec *recs = reinterpret_cast<Rec *>(smem + L::REC_OFF);
   volatile int *iq = reinterpret_cast<volatile int *>(smem + L::IQ_OFF);
 
@@ -183,6 +189,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(L::B_EE + t), 1);
     }
     *abort = 0;
+    // metadata whose build failed (a grid barrier that ran out, capacity) is
+    // not read at all: every CTA skips its work and the status is recorded
+    const long long ms = *p.meta_status;
+    *meta_bad = ms != ATTN_OK;
+    if (ms != ATTN_OK) atomicCAS(&g_fwd_status, 0u, static_cast<unsigned>(ms));
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -199,7 +210,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (*meta_bad) {
+    // nothing to do: no item is fetched, so the work counter stays at 0
+  } else if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t ld = 0, nonempty = 0, qpos = 0;
@@ -650,7 +663,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   if (warp == 9) tmem_dealloc(tmem, 512);
   if (threadIdx.x == 0) {
-    if (*abort) atomicExch(&g_fwd_status, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
+    if (*abort) atomicCAS(&g_fwd_status, 0u, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
     // every CTA has fetched its last item id once it gets here: the last one
     // to retire resets this launch's slot for its next use
     __threadfence();
@@ -691,13 +704,17 @@ static int launch_fwd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtens
                       const CUtensorMap &mo, const FwdParams &p, int grid, cudaStream_t s) {
   using L = Layout<D, NS>;
   static bool configured[kMaxDev] = {};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
-  if (!configured[dev]) {
-    if (cudaFuncSetAttribute(fwd_kernel<D, NS, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::ALLOC) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    configured[dev] = true;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(fwd_kernel<D, NS, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               L::ALLOC) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      configured[dev] = true;
+    }
   }
   fwd_kernel<D, NS, POLY><<<grid, NTHREADS, L::ALLOC, s>>>(mq, mk, mv, mo, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -744,6 +761,7 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   const int grid = static_cast<int>(items < sms ? items : sms);
   p.counter = next_counter();
   if (!p.counter) return ATTN_ERR_CUDA;
+  p.meta_status = reinterpret_cast<const long long *>(tiles->totals + 3);
   const int poly = g_exp2_poly;
   if (d == 128) {
     if (poly == 4) return launch_fwd<128, 3, 4>(mq, mk, mv, mo, p, grid, stream);
@@ -780,7 +798,7 @@ __global__ void selftest_timeout_kernel(unsigned long long wait_ns) {
   abort_flag = 0;
   fence_mbar_init();
   if (!mbar_wait_bounded(a, 0, reinterpret_cast<volatile int *>(&abort_flag), wait_ns))
-    atomicExch(&g_fwd_status, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
+    atomicCAS(&g_fwd_status, 0u, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
 }
 
 int selftest_timeout_launch(cudaStream_t s) {

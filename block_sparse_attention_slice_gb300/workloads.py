@@ -176,12 +176,23 @@ def gqa_causal_kv_split(S: int = 131072, H: int = 32, Hk: int = 8, n_split: int 
                     kv_splits=splits, sample_rows=True)
 
 
+def gqa_causal_32k() -> Workload:
+    """The long GQA causal problem at a quarter of its length: S=32768,
+    32 query heads / 8 KV heads, d=128, one causal slice, no KV split.  Its
+    inputs (470 MB) exceed L2, so it stands in for the S=131072 forward where
+    a profiler capture of the full size would hold too much device memory."""
+    w = gqa_causal_kv_split(S=32768)
+    return Workload("gqa_causal_s32768_h32_hk8_d128", w.S, w.H, w.Hk, w.d, w.scale, w.seed,
+                    slices=w.slices, sample_rows=True)
+
+
 ALL = {
     "tiny_causal": tiny_causal,
     "varlen_causal": varlen_causal,
     "block_sparse_strided": block_sparse_strided,
     "video_gen": video_gen,
     "gqa_causal": gqa_causal_kv_split,
+    "gqa_causal_32k": gqa_causal_32k,
 }
 
 

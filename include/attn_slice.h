@@ -71,7 +71,9 @@ typedef struct CUstream_st *attn_stream_t;
 #define ATTN_TILE_FULL   1   /* every pair valid: no per-element mask       */
 #define ATTN_TILE_MASKED 2   /* some pairs valid: masked from slice refs    */
                              /* Empty tiles have no entry at all            */
-/* ---- block-grid kinds (attn_slices_from_block_grid input) --------------- */
+/* ---- block-grid kinds (attn_slices_from_block_grid input; UltraAttn page,
+ * section 3: a block is Full when every position is valid, Causal when the
+ * positions on and below its diagonal are, Empty when none is) ----------- */
 #define ATTN_GRID_EMPTY  0
 #define ATTN_GRID_FULL   1
 #define ATTN_GRID_CAUSAL 2
@@ -92,7 +94,10 @@ typedef struct {
 } attn_slice_t;
 
 /* Tile metadata.  Filled by attn_build_tiles; every pointer points into the
- * caller's workspace on the device and stays valid while it lives.
+ * caller's workspace on the device and stays valid while it lives.  The
+ * status word totals[3] is ATTN_OK once the build has finished normally;
+ * attn_fwd and attn_bwd read it on the device and refuse metadata whose
+ * status is anything else (see attn_last_device_error).
  *   row_ptr [n_qtiles+1]  CSR row pointers over query tiles
  *   col_idx [nnz]         key-tile index, ascending within a query tile
  *   kind    [nnz]         ATTN_TILE_FULL or ATTN_TILE_MASKED
@@ -137,8 +142,13 @@ int attn_tiles_workspace_bytes(const attn_slice_t *h_slices, int n_slices, int s
  * one is copied to the start of d_ws (cudaMemcpyAsync on `stream`).  The
  * metadata is produced on `stream` by one cooperative kernel when every query
  * tile's CTA fits on the GPU at once, else by two kernels.  The counts are
- * exact integers, so the result is bit-identical run to run.  Errors: INVALID_ARG, OVERLAP,
- * UNSUPPORTED (tile or grid too large), CAPACITY (ws_bytes too small), CUDA. */
+ * exact integers, so the result is bit-identical run to run.  The cooperative
+ * kernel's grid-wide barrier is a bounded wait (attn_set_wait_limit_ns); if it
+ * runs out, every query tile gets an empty list, totals[0..2] are 0, totals[3]
+ * is ATTN_ERR_TIMEOUT and attn_last_device_error() reports TIMEOUT: the
+ * metadata stays safe to read and the kernels that use it refuse it.
+ * Errors: INVALID_ARG, OVERLAP, UNSUPPORTED (tile or grid too large),
+ * CAPACITY (ws_bytes too small), CUDA. */
 int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
                      int tile_q, int tile_k, void *d_ws, size_t ws_bytes,
                      attn_tiles_t *tiles, attn_stream_t stream);
@@ -154,7 +164,11 @@ int attn_build_tiles(const attn_slice_t *h_slices, int n_slices, int sq, int sk,
  * (ATTN_NOALLOC_MAX_QTILES entries, 20 bytes each, 320 KiB), which every GPU
  * that loads the library holds until the process exits.
  *   arguments   as attn_build_tiles; d_out (256-byte aligned) receives the
- *               metadata and needs out_bytes >= attn_tiles_workspace_bytes()
+ *               metadata and needs out_bytes >= attn_tiles_workspace_bytes():
+ *               the same size as attn_build_tiles' workspace, since the
+ *               metadata keeps that layout (its four counter regions are
+ *               simply left unused); only the counters move into the
+ *               library's array
  *   limits      ceil(sq / tile_q) <= ATTN_NOALLOC_MAX_QTILES, else CAPACITY
  * No cudaMalloc, cudaFree or other allocating call is made.  The first call
  * on a device looks up the array's device address once (cudaGetSymbolAddress,
@@ -173,9 +187,13 @@ int attn_build_tiles_noalloc(const attn_slice_t *h_slices, int n_slices, int sq,
  * synchronises `stream` first. */
 int attn_tiles_totals(const attn_tiles_t *tiles, int64_t h_totals[4], attn_stream_t stream);
 
-/* Full / Causal / Empty block grid -> slice list (host only).  One slice per
- * non-Empty block, in row-major block order: FULL -> a full slice of the
- * block, CAUSAL -> a causal slice of the block (requires block_q == block_k).
+/* Full / Causal / Empty block grid -> slice list (host only).  UltraAttn
+ * page, section 3: the attention matrix cut into (query chunk x key chunk)
+ * blocks, each Full (every position valid), Causal (only part valid: here
+ * the positions on and below the block's diagonal) or Empty (skipped).  One
+ * slice per non-Empty block, in row-major block order: FULL -> a full slice
+ * of the block, CAUSAL -> a causal slice of the block (requires
+ * block_q == block_k).
  *   h_grid     uint8 [nbq * nbk] of ATTN_GRID_*
  *   h_out      room for `capacity` slices; *n_out receives the count
  * Errors: INVALID_ARG (bad kind, causal on a non-square block), CAPACITY. */
@@ -194,10 +212,19 @@ int attn_slices_from_block_grid(const uint8_t *h_grid, int nbq, int nbk, int blo
  *               ATTN_FWD_TILE_Q x ATTN_FWD_TILE_K
  *   out         [sq, hq, d] of out_dtype (ATTN_DTYPE_BF16 or _F32)
  *   lse         [hq, sq] f32: ln sum exp(scale q.k) over valid keys
- * A query row with no valid key gets O = 0 and lse = -inf.
- * Errors: INVALID_ARG, UNSUPPORTED (d, tile shape, misaligned pointer), CUDA;
- * a stalled pipeline stage gives up after a bounded wait and is reported by
- * attn_last_device_error() as TIMEOUT. */
+ * A query row with no valid key gets O = 0 and lse = -inf.  q, k and v must
+ * not overlap out (INVALID_ARG).
+ * Each launch takes one of 4096 library-owned work counters in turn (a
+ * counter starts at 0 and the launch puts it back to 0 when it ends).  A
+ * launch captured in a CUDA graph keeps the counter it took, so replays of
+ * one captured launch must not run concurrently with each other, nor with
+ * the launch that takes the same counter 4096 launches later; otherwise two
+ * grids share one counter and rows come out wrong.
+ * Errors: INVALID_ARG, UNSUPPORTED (d, tile shape, misaligned pointer), CUDA.
+ * Errors found on the device are reported by attn_last_device_error(): a
+ * stalled pipeline stage gives up after a bounded wait (TIMEOUT), and
+ * metadata whose build did not finish with ATTN_OK is not read at all (its
+ * status); the outputs are then incomplete. */
 int attn_fwd(const void *q, const void *k, const void *v, int sq, int sk, int hq, int hk, int d,
              float scale, const attn_tiles_t *tiles, void *out, int out_dtype, float *lse,
              attn_stream_t stream);
@@ -233,16 +260,22 @@ int attn_merge(const void *const *h_o_parts, const float *const *h_lse_parts, in
  *   d_ws            >= attn_bwd_workspace_bytes() bytes (D, transposed lists)
  * No atomics: dK, dV are accumulated per key tile over its query tiles (a
  * transposed copy of the lists built on the device), dQ per query tile.
- * Errors: as attn_fwd, plus CAPACITY when ws_bytes is too small. */
+ * Errors: as attn_fwd (including the refusal of metadata whose status is not
+ * ATTN_OK), plus CAPACITY when ws_bytes is too small. */
 int attn_bwd_workspace_bytes(const attn_tiles_t *tiles, int hq, size_t *bytes);
 int attn_bwd(const void *q, const void *k, const void *v, const void *out, int out_dtype,
              const void *dout, const float *lse, int sq, int sk, int hq, int hk, int d, float scale,
              const attn_tiles_t *tiles, void *dq, void *dk, void *dv, int grad_dtype, void *d_ws,
              size_t ws_bytes, attn_stream_t stream);
 
-/* Synchronises `stream`, then returns and clears the device-side status of
- * the forward and backward kernels on the current device: ATTN_OK, or ATTN_ERR_TIMEOUT when
- * a bounded wait ran out (the kernel then left its outputs incomplete). */
+/* Synchronises `stream`, then returns and clears the device-side failure
+ * status of the metadata build, forward and backward kernels on the current
+ * device: ATTN_OK, ATTN_ERR_TIMEOUT when a bounded wait ran out (a build's
+ * grid barrier, a forward or backward pipeline stage), or the status of
+ * refused metadata.  The first failure of each kernel family is kept.  The
+ * status words are per device, not per stream: a caller that runs launches
+ * on several streams cannot tell from here which launch failed, and should
+ * synchronise all of them before reading. */
 int attn_last_device_error(attn_stream_t stream);
 
 /* Sets the bound on every device-side wait of later attn_fwd launches on the

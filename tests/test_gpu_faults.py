@@ -87,3 +87,92 @@ def test_overlap_check_agrees_with_brute_force(seed):
             assert e.value.code == B.ATTN_ERR_OVERLAP
         else:
             attn_build_tiles(sl, 2048, 2048).to_host()
+
+
+def _status_word(tiles):
+    """The metadata's totals[0..3] as an int64 view into its device workspace."""
+    return tiles._view(tiles.struct.totals, 4, torch.int64)
+
+
+def test_metadata_with_a_failed_status_is_refused():
+    # Metadata whose build did not finish with ATTN_OK -- made here on the
+    # host by writing CAPACITY into the status word of good metadata -- is
+    # not read by the forward or the backward: the forward leaves its outputs
+    # untouched, both report the status, and the same metadata with its
+    # status put back gives the original result bit for bit.
+    S, H, d = 1024, 2, 128
+    q, k, v = _qkv(S, H, H, d)
+    t = attn_build_tiles(np.array([[0, S, 0, S, 1]], np.int32), S, S)
+    ref_o, ref_l = attn_fwd(q, k, v, t, 0.1)
+    torch.cuda.synchronize()
+    assert attn_last_device_error() == 0
+    st = _status_word(t)
+    st[3] = B.ATTN_ERR_CAPACITY
+    out = torch.full_like(ref_o, 7.0)
+    lse = torch.full_like(ref_l, 7.0)
+    attn_fwd(q, k, v, t, 0.1, out=out, lse=lse)
+    assert attn_last_device_error() == B.ATTN_ERR_CAPACITY
+    assert torch.all(out == 7.0) and torch.all(lse == 7.0)
+    do = torch.ones_like(q)
+    B.attn_bwd(q, k, v, ref_o, do, ref_l, t, 0.1)
+    assert attn_last_device_error() == B.ATTN_ERR_CAPACITY
+    assert attn_last_device_error() == 0          # cleared by the read
+    st[3] = 0
+    o2, l2 = attn_fwd(q, k, v, t, 0.1)
+    torch.cuda.synchronize()
+    assert attn_last_device_error() == 0
+    assert torch.equal(o2.view(torch.int16), ref_o.view(torch.int16))
+    assert torch.equal(l2.view(torch.int32), ref_l.view(torch.int32))
+
+
+def test_short_wait_limit_times_out_the_forward_and_the_build():
+    # With a 1 us bound on every device wait, the pipeline waits of a long
+    # causal forward (the TMA producer waiting for a free ring slot, the
+    # softmax waiting for the next scores) and the grid barrier of a
+    # cooperative build whose 512 query tiles finish counting microseconds
+    # apart run out.  The kernels give up, let their in-flight copies and
+    # MMAs finish, free tensor memory and report TIMEOUT.  A build that gave
+    # up leaves every list empty with TIMEOUT as its status, which the
+    # forward refuses.  Afterwards, with the normal bound, the context works
+    # and the forward is bit-identical to the run made before.
+    S, H, Hk, d = 8192, 4, 2, 128
+    q, k, v = _qkv(S, H, Hk, d)
+    t = attn_build_tiles(np.array([[0, S, 0, S, 1]], np.int32), S, S)
+    ref_o, ref_l = attn_fwd(q, k, v, t, 0.088)
+    torch.cuda.synchronize()
+    assert attn_last_device_error() == 0
+    L = 131072
+    big = np.array([[0, L, 0, L, 1]], np.int32)
+    qb, kb, vb = _qkv(L, 1, 1, d)
+    fwd_rc, build_rc, refused = [], [], []
+    attn_set_wait_limit_ns(1000)
+    try:
+        for _ in range(3):
+            attn_fwd(q, k, v, t, 0.088)
+            fwd_rc.append(attn_last_device_error())
+            tb = attn_build_tiles(big, L, L)
+            rc = attn_last_device_error()
+            build_rc.append((rc, tb.totals()))
+            if rc == B.ATTN_ERR_TIMEOUT:
+                o = torch.full((L, 1, d), 3.0, dtype=torch.bfloat16, device="cuda")
+                attn_fwd(qb, kb, vb, tb, 0.088, out=o)
+                refused.append((attn_last_device_error(), bool(torch.all(o == 3.0))))
+    finally:
+        attn_set_wait_limit_ns(4_000_000_000)
+    assert set(fwd_rc) <= {0, B.ATTN_ERR_TIMEOUT} and B.ATTN_ERR_TIMEOUT in fwd_rc, fwd_rc
+    assert B.ATTN_ERR_TIMEOUT in [rc for rc, _ in build_rc], build_rc
+    for rc, tot in build_rc:
+        assert rc in (0, B.ATTN_ERR_TIMEOUT)
+        assert tot == ([0, 0, 0, B.ATTN_ERR_TIMEOUT] if rc else [tot[0], tot[1], tot[2], 0])
+    assert refused and all(r == (B.ATTN_ERR_TIMEOUT, True) for r in refused), refused
+    o2, l2 = attn_fwd(q, k, v, t, 0.088)
+    torch.cuda.synchronize()
+    assert attn_last_device_error() == 0
+    assert torch.equal(o2.view(torch.int16), ref_o.view(torch.int16))
+    assert torch.equal(l2.view(torch.int32), ref_l.view(torch.int32))
+    # and a build with the normal bound gives the causal mask's closed-form
+    # totals: query tile i (256 rows) meets key tiles 0 .. 2i+1 (128 keys),
+    # the last two MASKED, each referencing the one slice
+    tb = attn_build_tiles(big, L, L)
+    assert tb.totals() == [sum(2 * i + 2 for i in range(L // 256)), 2 * (L // 256),
+                           L * (L + 1) // 2, 0]

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from block_sparse_attention_slice_gb300 import binding as B
 from block_sparse_attention_slice_gb300 import workloads as W
 
@@ -33,23 +34,31 @@ def _noalloc(slices, sq, sk, tq, tk):
     return B.attn_build_tiles_noalloc(slices, sq, sk, out, tq, tk).to_host()
 
 
-def test_two_calls_in_a_row_match_the_workspace_build():
+# "1": count and fill as two launches, which hand the counters over through
+# the library's array; "0": one cooperative launch where every query tile's
+# CTA fits at once (the variable is read on every call)
+@pytest.mark.parametrize("two_launch", ["0", "1"])
+def test_two_calls_in_a_row_match_the_workspace_build(two_launch, monkeypatch):
+    monkeypatch.setenv("ATTN_BUILD_TWO_LAUNCH", two_launch)
     cases = [(W.video_slices(), 65536, 65536, 256, 128),
              (W.random_slices(3000, 2500, 40, seed=21, unit=1, max_len=600), 3000, 2500, 64, 32)]
     for sl, sq, sk, tq, tk in cases:
         ref = B.attn_build_tiles(sl, sq, sk, tq, tk).to_host()
+        _same(ref, oracle.oracle_tiles(sl, sq, sk, tq, tk))
         first = _noalloc(sl, sq, sk, tq, tk)
         second = _noalloc(sl, sq, sk, tq, tk)
         _same(first, ref)
         _same(second, ref)
 
 
-def test_previous_contents_do_not_leak_into_a_smaller_build():
+@pytest.mark.parametrize("two_launch", ["0", "1"])
+def test_previous_contents_do_not_leak_into_a_smaller_build(two_launch, monkeypatch):
+    monkeypatch.setenv("ATTN_BUILD_TWO_LAUNCH", two_launch)
     big = W.random_slices(8192, 8192, 60, seed=5, unit=16, max_len=64)
     small = np.array([[0, 700, 0, 700, 1], [700, 900, 0, 300, 3]], np.int32)
     _noalloc(big, 8192, 8192, 128, 128)
     got = _noalloc(small, 900, 900, 256, 128)
-    _same(got, B.attn_build_tiles(small, 900, 900, 256, 128).to_host())
+    _same(got, oracle.oracle_tiles(small, 900, 900, 256, 128))
 
 
 def test_rejects_more_query_tiles_than_the_array_holds():
