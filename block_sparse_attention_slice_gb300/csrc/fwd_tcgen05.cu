@@ -46,6 +46,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 #include <type_traits>
 
@@ -87,6 +88,7 @@ struct FwdParams {
   unsigned long long wait_ns;
   unsigned int *counter;          // this launch's work counter (0 at launch, reset by its last CTA)
   const long long *meta_status;   // the metadata build's status word (totals[3])
+  int test_stall;                 // failure-path test: leave one ring slot unarmed (see below)
 };
 
 // One resolved tile entry: key tile, kind, reference range and up to two
@@ -254,6 +256,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
+          // failure-path test only: the CTA's second K/V load (V of its first
+          // step) is neither armed nor issued, so the MMA lane's bounded wait
+          // for that slot runs out and the whole abort path runs
+          if (p.test_stall && ld == 1) continue;
           mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::TILE);
           for (int hh = 0; hh < L::NHALF; ++hh)
             tma_load_2d(kv_smem + slot * L::TILE + hh * L::HALF, (i & 1) ? &tm_v : &tm_k,
@@ -762,6 +768,12 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   p.counter = next_counter();
   if (!p.counter) return ATTN_ERR_CUDA;
   p.meta_status = reinterpret_cast<const long long *>(tiles->totals + 3);
+  // ATTN_TEST_STALL_FWD=1 in the environment: every CTA leaves its second
+  // K/V load unissued, so the launch ends by its bounded waits running out
+  // (ATTN_ERR_TIMEOUT) -- the form in which the tests drive the forward's
+  // own abort path without faulting or hanging the GPU
+  const char *stall = std::getenv("ATTN_TEST_STALL_FWD");
+  p.test_stall = stall && stall[0] == '1';
   const int poly = g_exp2_poly;
   if (d == 128) {
     if (poly == 4) return launch_fwd<128, 3, 4>(mq, mk, mv, mo, p, grid, stream);

@@ -86,3 +86,48 @@ def test_keys_without_queries_get_zero_gradient():
     dq, dk, dv = attn_bwd(q, k, v, out, do, lse, tiles, 0.09)
     assert torch.all(dk[1024:1536] == 0) and torch.all(dv[1024:1536] == 0)
     assert torch.any(dk[:1024] != 0) and torch.any(dv[1536:] != 0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["varlen_causal", "block_sparse_strided"])
+def test_workload_scale_sampled(name):
+    # The backward at the size ``bench.py --pass bwd`` times, in the same
+    # launch configuration: the transposed per-key-tile lists and the long
+    # dK/dV walks of the packed documents (S = 16384) and of the block-sparse
+    # grid (S = 32768, whose sink column 0 is reached by every query).  dK and
+    # dV are compared at 512 seeded keys (plus key 0 and tile edges) of four
+    # KV heads, dQ at 512 seeded rows of the same heads, against the sampled
+    # form of the backward oracle.
+    from oracle.backward import oracle_attention_backward_sampled
+    from block_sparse_attention_slice_gb300 import attn_slices_from_block_grid
+    from parity import THREADS, mask_fn
+    w = W.ALL[name]()
+    sl = attn_slices_from_block_grid(w.grid, w.block, w.block) if w.grid is not None else w.slices
+    q, k, v = W.draw_qkv(w.S, w.H, w.Hk, w.d, w.seed)
+    rng = np.random.default_rng(w.seed + 1)
+    do = torch.from_numpy(rng.standard_normal((w.S, w.H, w.d), dtype=np.float32)).to(torch.bfloat16)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    tiles = attn_build_tiles(sl, w.S, w.S)
+    out, lse = attn_fwd(qd, kd, vd, tiles, w.scale, out_dtype=torch.float32)
+    dq, dk, dv = attn_bwd(qd, kd, vd, out, dod, lse, tiles, w.scale)
+    torch.cuda.synchronize()
+    heads = [0, 5, 10, 15]
+    assert w.H == w.Hk            # one query head per KV head: heads double as groups
+    mask = mask_fn(w)
+    fwd = oracle.oracle_attention(f64(q), f64(k), f64(v), w.scale, mask, heads=heads,
+                                  threads=min(THREADS, len(heads)))
+    pick = np.random.default_rng(321)
+    edges = [0, 1, 127, 128, w.S // 2, w.S - 1]
+    keys = {g: np.unique(np.concatenate([pick.choice(w.S, 512, replace=False), edges]))
+            for g in heads}
+    rows = {h: np.unique(np.concatenate([pick.choice(w.S, 512, replace=False), edges]))
+            for h in heads}
+    sk, sv, sq = oracle_attention_backward_sampled(f64(q), f64(k), f64(v), f64(do), w.scale, mask,
+                                                   fwd, keys, rows)
+    dkc, dvc, dqc = dk.cpu(), dv.cpu(), dq.cpu()
+    for g in heads:
+        J = torch.as_tensor(keys[g])
+        _check(f"dk head {g}", dkc[J, g], sk[g])
+        _check(f"dv head {g}", dvc[J, g], sv[g])
+        R = torch.as_tensor(rows[g])
+        _check(f"dq head {g}", dqc[R, g], sq[g])

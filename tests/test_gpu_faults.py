@@ -125,31 +125,21 @@ def test_metadata_with_a_failed_status_is_refused():
     assert torch.equal(l2.view(torch.int32), ref_l.view(torch.int32))
 
 
-def test_short_wait_limit_times_out_the_forward_and_the_build():
-    # With a 1 us bound on every device wait, the pipeline waits of a long
-    # causal forward (the TMA producer waiting for a free ring slot, the
-    # softmax waiting for the next scores) and the grid barrier of a
-    # cooperative build whose 512 query tiles finish counting microseconds
-    # apart run out.  The kernels give up, let their in-flight copies and
-    # MMAs finish, free tensor memory and report TIMEOUT.  A build that gave
-    # up leaves every list empty with TIMEOUT as its status, which the
-    # forward refuses.  Afterwards, with the normal bound, the context works
-    # and the forward is bit-identical to the run made before.
-    S, H, Hk, d = 8192, 4, 2, 128
-    q, k, v = _qkv(S, H, Hk, d)
-    t = attn_build_tiles(np.array([[0, S, 0, S, 1]], np.int32), S, S)
-    ref_o, ref_l = attn_fwd(q, k, v, t, 0.088)
-    torch.cuda.synchronize()
-    assert attn_last_device_error() == 0
-    L = 131072
+def test_short_wait_limit_times_out_the_build_barrier():
+    # With a 1 us bound, the grid barrier of a cooperative build whose 512
+    # query tiles finish counting microseconds apart runs out (the barrier
+    # polls the global timer directly).  Every CTA then follows one "abort"
+    # decision: every list is left empty, the totals are zero and the status
+    # is TIMEOUT, which the forward refuses without writing its outputs.
+    # With the normal bound the same build gives the causal mask's
+    # closed-form totals.
+    d, L = 128, 131072
     big = np.array([[0, L, 0, L, 1]], np.int32)
     qb, kb, vb = _qkv(L, 1, 1, d)
-    fwd_rc, build_rc, refused = [], [], []
+    build_rc, refused = [], []
     attn_set_wait_limit_ns(1000)
     try:
         for _ in range(3):
-            attn_fwd(q, k, v, t, 0.088)
-            fwd_rc.append(attn_last_device_error())
             tb = attn_build_tiles(big, L, L)
             rc = attn_last_device_error()
             build_rc.append((rc, tb.totals()))
@@ -159,20 +149,47 @@ def test_short_wait_limit_times_out_the_forward_and_the_build():
                 refused.append((attn_last_device_error(), bool(torch.all(o == 3.0))))
     finally:
         attn_set_wait_limit_ns(4_000_000_000)
-    assert set(fwd_rc) <= {0, B.ATTN_ERR_TIMEOUT} and B.ATTN_ERR_TIMEOUT in fwd_rc, fwd_rc
     assert B.ATTN_ERR_TIMEOUT in [rc for rc, _ in build_rc], build_rc
     for rc, tot in build_rc:
         assert rc in (0, B.ATTN_ERR_TIMEOUT)
         assert tot == ([0, 0, 0, B.ATTN_ERR_TIMEOUT] if rc else [tot[0], tot[1], tot[2], 0])
     assert refused and all(r == (B.ATTN_ERR_TIMEOUT, True) for r in refused), refused
-    o2, l2 = attn_fwd(q, k, v, t, 0.088)
-    torch.cuda.synchronize()
-    assert attn_last_device_error() == 0
-    assert torch.equal(o2.view(torch.int16), ref_o.view(torch.int16))
-    assert torch.equal(l2.view(torch.int32), ref_l.view(torch.int32))
-    # and a build with the normal bound gives the causal mask's closed-form
-    # totals: query tile i (256 rows) meets key tiles 0 .. 2i+1 (128 keys),
-    # the last two MASKED, each referencing the one slice
+    # query tile i (256 rows) meets key tiles 0 .. 2i+1 (128 keys), the last
+    # two MASKED, each referencing the one slice
     tb = attn_build_tiles(big, L, L)
     assert tb.totals() == [sum(2 * i + 2 for i in range(L // 256)), 2 * (L // 256),
                            L * (L + 1) // 2, 0]
+    assert attn_last_device_error() == 0
+
+
+def test_forward_wait_that_never_completes_aborts_cleanly(monkeypatch):
+    # The forward's own abort path, driven by a barrier that nothing
+    # completes: with ATTN_TEST_STALL_FWD=1 every CTA leaves its second K/V
+    # load unissued, so the MMA lane's bounded wait for that ring slot runs
+    # out (50 ms here).  The CTA then raises its abort flag, the producer
+    # lets its issued loads land, the MMA lane waits for its issued MMAs, the
+    # softmax warps leave their waits, tensor memory is freed and the last
+    # CTA resets the work counter; the launch reports TIMEOUT.  Afterwards,
+    # without the switch and with the normal bound, the forward on the same
+    # inputs is bit-identical to a run made before the test.
+    S, H, Hk, d = 8192, 4, 2, 128
+    q, k, v = _qkv(S, H, Hk, d)
+    t = attn_build_tiles(np.array([[0, S, 0, S, 1]], np.int32), S, S)
+    ref_o, ref_l = attn_fwd(q, k, v, t, 0.088)
+    torch.cuda.synchronize()
+    assert attn_last_device_error() == 0
+    attn_set_wait_limit_ns(50_000_000)
+    monkeypatch.setenv("ATTN_TEST_STALL_FWD", "1")
+    try:
+        attn_fwd(q, k, v, t, 0.088)
+        rc = attn_last_device_error()
+    finally:
+        monkeypatch.delenv("ATTN_TEST_STALL_FWD")
+        attn_set_wait_limit_ns(4_000_000_000)
+    assert rc == B.ATTN_ERR_TIMEOUT
+    for _ in range(2):
+        o2, l2 = attn_fwd(q, k, v, t, 0.088)
+        torch.cuda.synchronize()
+        assert attn_last_device_error() == 0
+        assert torch.equal(o2.view(torch.int16), ref_o.view(torch.int16))
+        assert torch.equal(l2.view(torch.int32), ref_l.view(torch.int32))

@@ -55,3 +55,37 @@ def test_delta_identity_and_empty_rows():
     # keys 8..15 are valid for no row -> no gradient reaches them
     assert np.all(dk[8:] == 0) and np.all(dv[8:] == 0)
     assert np.any(dk[:8] != 0) and np.any(dv[:8] != 0)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_sampled_gradients_equal_the_dense_ones(seed):
+    # The sampled form (P rebuilt from the forward oracle's LSE, keys visited
+    # column by column over row blocks) must reproduce the dense backward --
+    # itself pinned by finite differences above -- at every sampled position:
+    # all four slice kinds, grouped heads, rows and keys that no pair reaches.
+    from oracle.backward import oracle_attention_backward_sampled
+    rng = np.random.default_rng(seed + 7)
+    S_q, S_k, H, Hk, d = 90, 110, 4, 2, 8
+    sl = W.random_slices(S_q, S_k, 12, seed=seed + 60, unit=1, max_len=40)
+    m = lambda r: mask_rows(sl, r, S_k)
+    q = rng.standard_normal((S_q, H, d)); k = rng.standard_normal((S_k, Hk, d))
+    v = rng.standard_normal((S_k, Hk, d)); G = rng.standard_normal((S_q, H, d))
+    scale = 0.4
+    dq, dk, dv, _ = oracle_attention_backward(q, k, v, G, scale, m)
+    fwd = oracle_attention(q, k, v, scale, m)
+    keys = {g: np.sort(rng.choice(S_k, 30, replace=False)) for g in range(Hk)}
+    rows = {h: np.sort(rng.choice(S_q, 25, replace=False)) for h in range(H)}
+    sk, sv, sq = oracle_attention_backward_sampled(q, k, v, G, scale, m, fwd, keys, rows, row_block=16)
+    for g, J in keys.items():
+        np.testing.assert_allclose(sk[g], dk[J, g, :], atol=1e-12, rtol=1e-10)
+        np.testing.assert_allclose(sv[g], dv[J, g, :], atol=1e-12, rtol=1e-10)
+    for h, R in rows.items():
+        np.testing.assert_allclose(sq[h], dq[R, h, :], atol=1e-12, rtol=1e-10)
+    # positions that no valid pair reaches come out exactly zero
+    M = m(np.arange(S_q))
+    dead_k = np.nonzero(~M.any(axis=0))[0]
+    dead_q = np.nonzero(~M.any(axis=1))[0]
+    assert dead_k.size and dead_q.size
+    sk2, sv2, sq2 = oracle_attention_backward_sampled(q, k, v, G, scale, m, fwd,
+                                                      {0: dead_k}, {0: dead_q})
+    assert np.all(sk2[0] == 0) and np.all(sv2[0] == 0) and np.all(sq2[0] == 0)
