@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="leave out the forward timings of the other workloads (the 'configs' key)")
+    ap.add_argument("--fwd-tile-q", type=int, default=256, choices=[256, 512],
+                    help="query rows per forward work item: 256 = single-CTA kernel (default); "
+                         "512 = CTA-pair kernel (two CTAs share each M=256 MMA; head dim 128)")
     ap.add_argument("--exp2-poly", type=int, default=0, choices=[0, 4, 8],
                     help="forward exponentials: 0 all on the special-function unit (default); "
                          "4 / 8 every 4th / 8th pair of a FULL tile on the FMA-pipe polynomial")
@@ -305,14 +308,15 @@ def gpu_arm(args, ws, rank, local):
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
     prep = B.host_slices(sl)
-    ws_bytes = pkg.attn_tiles_workspace_bytes(sl, w.S, w.S, 256, 128)
+    tq = args.fwd_tile_q
+    ws_bytes = pkg.attn_tiles_workspace_bytes(sl, w.S, w.S, tq, 128)
     wsbuf = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty((w.S, w.H, w.d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.H, w.S), dtype=torch.float32, device=dev)
     split = []
     for s2 in w.kv_splits:
         p2 = B.host_slices(s2)
-        b2 = torch.empty(pkg.attn_tiles_workspace_bytes(s2, w.S, w.S, 256, 128), dtype=torch.uint8, device=dev)
+        b2 = torch.empty(pkg.attn_tiles_workspace_bytes(s2, w.S, w.S, tq, 128), dtype=torch.uint8, device=dev)
         split.append((s2, p2, b2, torch.empty((w.S, w.H, w.d), dtype=torch.float32, device=dev),
                       torch.empty((w.H, w.S), dtype=torch.float32, device=dev)))
     mout = torch.empty_like(out) if split else None
@@ -320,7 +324,7 @@ def gpu_arm(args, ws, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    tiles0 = pkg.attn_build_tiles(sl, w.S, w.S, ws=wsbuf, prepared=prep)
+    tiles0 = pkg.attn_build_tiles(sl, w.S, w.S, tq, ws=wsbuf, prepared=prep)
     nnz, nref, pairs_per_head, status = tiles0.totals()
     assert status == 0
     flops = 4.0 * w.d * pairs_per_head * w.H
@@ -332,7 +336,7 @@ def gpu_arm(args, ws, rank, local):
     def step(qx, kx, vx, ev=None):
         if ev is not None:
             ev[0].record(stream)
-        t = pkg.attn_build_tiles(sl, w.S, w.S, ws=wsbuf, prepared=prep)
+        t = pkg.attn_build_tiles(sl, w.S, w.S, tq, ws=wsbuf, prepared=prep)
         if ev is not None:
             ev[1].record(stream)
         pkg.attn_fwd(qx, kx, vx, t, w.scale, out=out, lse=lse)
@@ -341,7 +345,7 @@ def gpu_arm(args, ws, rank, local):
         if split:
             parts = []
             for s2, p2, b2, o2, l2 in split:
-                t2 = pkg.attn_build_tiles(s2, w.S, w.S, ws=b2, prepared=p2)
+                t2 = pkg.attn_build_tiles(s2, w.S, w.S, tq, ws=b2, prepared=p2)
                 pkg.attn_fwd(qx, kx, vx, t2, w.scale, out=o2, lse=l2)
                 parts.append((o2, l2))
             if ev is not None:
@@ -421,13 +425,13 @@ def gpu_arm(args, ws, rank, local):
                 sx["q"].copy_(qh, non_blocking=True)
                 sx["k"].copy_(kh, non_blocking=True)
                 sx["v"].copy_(vh, non_blocking=True)
-                t = pkg.attn_build_tiles(sl, w.S, w.S, ws=sx["ws"], prepared=prep)
+                t = pkg.attn_build_tiles(sl, w.S, w.S, tq, ws=sx["ws"], prepared=prep)
                 pkg.attn_fwd(sx["q"], sx["k"], sx["v"], t, w.scale, out=sx["out"], lse=sx["lse"])
                 res, resl = sx["out"], sx["lse"]
                 if split:
                     parts = []
                     for s2, p2, b2, o2, l2 in sx["split"]:
-                        t2 = pkg.attn_build_tiles(s2, w.S, w.S, ws=b2, prepared=p2)
+                        t2 = pkg.attn_build_tiles(s2, w.S, w.S, tq, ws=b2, prepared=p2)
                         pkg.attn_fwd(sx["q"], sx["k"], sx["v"], t2, w.scale, out=o2, lse=l2)
                         parts.append((o2, l2))
                     pkg.attn_merge([x[0] for x in parts], [x[1] for x in parts], out=sx["mout"], lse=sx["mlse"])
@@ -496,7 +500,7 @@ def gpu_arm(args, ws, rank, local):
 
     if not args.no_configs:
         extra["configs"] = side_workloads(pkg, W, dev, flush, pk, pk_src,
-                                          [x for x in SIDE_WORKLOADS if x != args.workload])
+                                          [x for x in SIDE_WORKLOADS if x != args.workload], tq)
         barrier(ws)
 
     cpu = None
@@ -521,6 +525,8 @@ def gpu_arm(args, ws, rank, local):
                                    "build + forward",
                            "l2": "flushed between timed steps",
                            "exp2_poly": args.exp2_poly,
+                           "fwd_kernel": ("CTA pair (512-row items, cta_group::2)" if tq == 512
+                                          else "single CTA (256-row items)"),
                            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
                 "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16_tflops"],
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
@@ -528,7 +534,7 @@ def gpu_arm(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def side_workloads(pkg, W, dev, flush, pk, pk_src, names, reps=10):
+def side_workloads(pkg, W, dev, flush, pk, pk_src, names, tq=256, reps=10):
     """Event-timed forward (inputs resident, L2 flushed before each launch) of
     each named workload: TFLOP/s on valid pairs and its fraction of the burst
     tensor peak (these kernels run for well under a second)."""
@@ -539,7 +545,7 @@ def side_workloads(pkg, W, dev, flush, pk, pk_src, names, reps=10):
         sl = slices_of(w)
         q, k, v = W.draw_qkv(w.S, w.H, w.Hk, w.d, w.seed)
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-        tiles = pkg.attn_build_tiles(sl, w.S, w.S)
+        tiles = pkg.attn_build_tiles(sl, w.S, w.S, tq)
         nnz, _, pairs, status = tiles.totals()
         assert status == 0
         out = torch.empty((w.S, w.H, w.d), dtype=torch.bfloat16, device=dev)

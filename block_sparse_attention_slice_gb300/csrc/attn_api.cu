@@ -290,7 +290,8 @@ int attn_fwd(const void *q, const void *k, const void *v, int sq, int sk, int hq
   if (out_dtype != ATTN_DTYPE_BF16 && out_dtype != ATTN_DTYPE_F32) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (tiles->sq != sq || tiles->sk != sk || !tiles->row_ptr) return ATTN_ERR_INVALID_ARG;
-  if (tiles->tile_q != ATTN_FWD_TILE_Q || tiles->tile_k != ATTN_FWD_TILE_K)
+  if (tiles->tile_k != ATTN_FWD_TILE_K ||
+      !(tiles->tile_q == ATTN_FWD_TILE_Q || (tiles->tile_q == ATTN_FWD_PAIR_TILE_Q && d == 128)))
     return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_UNSUPPORTED;
   // q, k, v (read through TMA while O is written) must not overlap out

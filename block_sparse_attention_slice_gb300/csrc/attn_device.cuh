@@ -22,6 +22,14 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile
   return __all_sync(0xffffffffu, ok);
 }
 
+// wait_all with a cluster-scope acquire (barriers the other CTA of a pair
+// completes).
+__device__ __forceinline__ bool wait_all_cl(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            uint64_t limit) {
+  bool ok = mbar_wait_bounded_cl(bar, parity, abort, limit);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Waits for in-flight asynchronous work before tensor memory and shared
 // memory are released on the failure path; bounded independently of *abort.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -118,14 +126,15 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tma_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map over a [rows, cols] row-major matrix, 64 x 128 boxes with
-// the 128-byte swizzle the MMA descriptors expect.
-inline int make_tma_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows) {
+// 2-D bf16 map over a [rows, cols] row-major matrix, boxes of 64 columns x
+// box_rows rows with the 128-byte swizzle the MMA descriptors expect.
+inline int make_tma_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                       uint32_t box_rows = 128) {
   auto enc = tma_encode_fn();
   if (!enc) return ATTN_ERR_CUDA;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

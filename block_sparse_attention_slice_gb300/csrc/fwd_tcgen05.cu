@@ -100,14 +100,19 @@ struct __align__(16) Rec {
 };
 static_assert(sizeof(Rec) == 64, "record size");
 
-template <int D, int NS>
+template <int D, int NS, bool PAIR>
 struct Layout {
   static constexpr int HALF = 128 * 64 * 2;          // 128 rows x 64 bf16 (one swizzle span)
   static constexpr int NHALF = D / 64;
   static constexpr int TILE = NHALF * HALF;          // 128 x D bf16
+  // a K/V ring slot holds a whole 128-key tile, or in a CTA pair this CTA's
+  // half of it: 64 keys x D of K (D/64 spans of 64 rows), or all 128 keys x
+  // D/2 columns of V (one span)
+  static constexpr int KVSLOT = PAIR ? TILE / 2 : TILE;
+  static constexpr int KSPAN = PAIR ? 64 * 128 : HALF;   // one 64-column span of a K slot
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TILE;
-  static constexpr int ST_OFF = KV_OFF + NS * TILE;   // bf16 O staging: one 128 x D tile per MMA tile
+  static constexpr int ST_OFF = KV_OFF + NS * KVSLOT;  // bf16 O staging: one 128 x D tile per MMA tile
   static constexpr int REC_OFF = ST_OFF + 2 * TILE;
   static constexpr int IQ_OFF = REC_OFF + RING * 64;
   static constexpr int BAR_OFF = IQ_OFF + IQ * 16;
@@ -121,7 +126,8 @@ struct Layout {
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;
-  static_assert(ST_OFF % 1024 == 0, "swizzled staging alignment");
+  static_assert(ST_OFF % 1024 == 0 && KVSLOT % 1024 == 0, "swizzled staging alignment");
+  static_assert(!PAIR || D == 128, "the CTA-pair kernel splits V into two 64-column spans");
   static_assert(ALLOC <= 232448, "shared memory per CTA");
 };
 
@@ -129,11 +135,21 @@ struct Item {
   int qt, h, g, e0, n;
 };
 
+// Work item -> (query tile, head).  Items run KV-head-group-major: all items
+// of KV head 0's group first (query tiles in longest-processing-time order,
+// for each query tile the group's query heads in turn), then group 1, and so
+// on.  The CTAs working at any moment then sweep the keys and values of one
+// or two KV heads (67 MB at S = 131072, d = 128), which stay in L2, instead
+// of those of every head; the order within a group, and the shortest items
+// coming last overall, keep the balance of the longest-processing-time order.
 __device__ __forceinline__ Item decode(const FwdParams &p, int item) {
   Item it;
-  it.qt = __ldg(p.sched + item / p.hq);
-  it.h = item % p.hq;
-  it.g = it.h / (p.hq / p.hk);
+  const int G = p.hq / p.hk;             // query heads per KV head
+  const int per_group = p.n_items / p.hk;
+  it.g = item / per_group;
+  const int r = item - it.g * per_group;
+  it.qt = __ldg(p.sched + r / G);
+  it.h = it.g * G + r % G;
   it.e0 = __ldg(p.row_ptr + it.qt);
   it.n = __ldg(p.row_ptr + it.qt + 1) - it.e0;
   return it;
@@ -142,12 +158,26 @@ __device__ __forceinline__ Item decode(const FwdParams &p, int item) {
 // POLY = 0: every exponential on the special-function unit; POLY = k > 0:
 // on FULL tiles, every k-th pair of a row's exponentials on the FMA-pipe
 // polynomial (exp2_poly2), the rest on the special-function unit.
-template <int D, int NS, int POLY>
+// PAIR: the CTA-pair form (FlashAttention-4 page, 2-CTA MMA: two CTAs share
+// one MMA and each loads half of the operand it shares).  A cluster of two
+// CTAs runs each work item of 512 query rows: MMA tile t covers rows
+// [256 t, 256 t + 256) of the item, of which CTA r holds rows 128 r .. 128 r
+// + 127 (its Q, its S, P and O in its own tensor memory, its own softmax and
+// epilogue).  Rank 0's MMA lane issues M = 256 MMAs for both CTAs: QK^T
+// takes keys [0, 64) of the key tile from rank 0's shared memory and [64,
+// 128) from rank 1's, P V takes V's columns [0, 64) from rank 0 and [64, 128)
+// from rank 1.  So each CTA loads half of every K/V tile and its MMA operand
+// traffic from shared memory for B is halved.  Both CTAs' loads and P
+// arrivals count on rank 0's barriers; rank 0's commits arrive on both.
+template <int D, int NS, int POLY, bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const FwdParams p) {
-  using L = Layout<D, NS>;
+  using L = Layout<D, NS, PAIR>;
+  static_assert(!PAIR || POLY == 0, "the CTA-pair kernel keeps every exponential on MUFU");
+  constexpr int ITEM_ROWS = PAIR ? 512 : 256;   // query rows of a work item
+  constexpr int TILE_ROWS = PAIR ? 256 : 128;   // query rows of one MMA tile
   static_assert(POLY == 0 || (POLY > 0 && 16 % POLY == 0), "polynomial period");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -163,6 +193,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_ns;
   const uint32_t q_smem = sb + L::Q_OFF, kv_smem = sb + L::KV_OFF;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  // barrier i of the pair's rank-0 CTA, as a cluster address (arrivals and
+  // load completions of both CTAs count there)
+  const uint32_t lbar0 = PAIR ? mapa_shared(sb + L::BAR_OFF, 0) : sb + L::BAR_OFF;
+  auto lbar = [&](int i) -> uint32_t { return lbar0 + 8u * i; };
+  // waits on barriers the other CTA of a pair may complete acquire at
+  // cluster scope
+  auto waitb = [&](uint32_t b, uint32_t par) -> bool {
+    if constexpr (PAIR) return mbar_wait_bounded_cl(b, par, abort, lim);
+    else return mbar_wait_bounded(b, par, abort, lim);
+  };
+  auto waitw = [&](uint32_t b, uint32_t par) -> bool {
+    if constexpr (PAIR) return wait_all_cl(b, par, abort, lim);
+    else return wait_all(b, par, abort, lim);
+  };
+  // rank 0's tensor-core commits arrive on both CTAs of a pair
+  auto commit = [&](uint32_t b) {
+    if constexpr (PAIR) mma_commit_pair_mc(b, 3);
+    else mma_commit(b);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_Q), 1);
@@ -173,7 +224,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::B_S + t), 1);
-      mbar_init(bar(L::B_P + t), 128);
+      // one arrival per softmax thread; in a pair one per softmax warp of
+      // either CTA (after a warp-wide sync)
+      mbar_init(bar(L::B_P + t), PAIR ? 8 : 128);
       mbar_init(bar(L::B_O + t), 1);
     }
     mbar_init(bar(L::B_DRAIN), 1);
@@ -181,10 +234,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(L::B_RF + r), 1);
       mbar_init(bar(L::B_RE + r), 8);
     }
-    // item ids are read by the MMA lane, the metadata warp and 8 softmax warps
+    // item ids are read by the MMA lane, the metadata warp and 8 softmax warps;
+    // in a pair, rank 0's queue slot is freed by both CTAs' readers (rank 1's
+    // producer, metadata warp and softmax warps; its MMA warp issues nothing)
     for (int u = 0; u < IQ; ++u) {
       mbar_init(bar(L::B_IF + u), 1);
-      mbar_init(bar(L::B_IE + u), 10);
+      mbar_init(bar(L::B_IE + u), PAIR ? 20 : 10);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::B_EF + t), 128);
@@ -199,8 +254,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_mbar_init();
   }
   if (warp == 9) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), 512);
+      tmem_relinquish();
+    }
   }
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_q);
@@ -209,6 +269,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -222,26 +283,47 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       while (ok) {
         // fetch the next item and publish it to the other roles
         const int qs = qpos % IQ;
-        if (qpos >= IQ && !mbar_wait_bounded(bar(L::B_IE + qs), (qpos / IQ - 1) & 1, abort, lim)) {
-          ok = false;
-          break;
+        int item;
+        if (leader) {
+          if (qpos >= IQ && !waitb(bar(L::B_IE + qs), (qpos / IQ - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          item = static_cast<int>(atomicAdd(p.counter, 1u));
+          iq[qs] = item;
+          if constexpr (PAIR) {
+            // publish to rank 1's queue as well
+            st_shared_cluster_u32(mapa_shared(sb + L::IQ_OFF + 4u * qs, 1), static_cast<uint32_t>(item));
+            mbar_arrive_cluster(mapa_shared(bar(L::B_IF + qs), 1));
+          }
+          mbar_arrive(bar(L::B_IF + qs));
+        } else {
+          // rank 1 of a pair: the item rank 0 published
+          if (!waitb(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
+            ok = false;
+            break;
+          }
+          item = iq[qs];
+          mbar_arrive_cluster(lbar(L::B_IE + qs));
         }
-        const int item = static_cast<int>(atomicAdd(p.counter, 1u));
-        iq[qs] = item;
-        mbar_arrive(bar(L::B_IF + qs));
         ++qpos;
         if (item >= p.n_items) break;
         const Item it = decode(p, item);
         if (it.n == 0) continue;
-        if (nonempty > 0 && !mbar_wait_bounded(bar(L::B_QE), (nonempty - 1) & 1, abort, lim)) {
+        if (nonempty > 0 && !waitb(bar(L::B_QE), (nonempty - 1) & 1)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::TILE);
+        // Q of this CTA's rows of both MMA tiles (in a pair rank 0 expects both CTAs' bytes)
+        if (leader) mbar_arrive_expect_tx(bar(L::B_Q), (PAIR ? 4 : 2) * L::TILE);
         for (int t = 0; t < 2; ++t)
-          for (int hh = 0; hh < L::NHALF; ++hh)
-            tma_load_2d(q_smem + t * L::TILE + hh * L::HALF, &tm_q, bar(L::B_Q), it.h * D + hh * 64,
-                        it.qt * 256 + t * BM);
+          for (int hh = 0; hh < L::NHALF; ++hh) {
+            const int y = it.qt * ITEM_ROWS + t * TILE_ROWS + static_cast<int>(rank) * BM;
+            if constexpr (PAIR)
+              tma_load_2d_pair(q_smem + t * L::TILE + hh * L::HALF, &tm_q, lbar(L::B_Q), it.h * D + hh * 64, y);
+            else
+              tma_load_2d(q_smem + t * L::TILE + hh * L::HALF, &tm_q, bar(L::B_Q), it.h * D + hh * 64, y);
+          }
         ++nonempty;
         // key-tile index of the next entry is fetched one entry ahead
         int kt = 0, kt_next = __ldg(p.col_idx + it.e0);
@@ -252,7 +334,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           const int slot = ld % NS;
           const uint32_t use = ld / NS;
-          if (use > 0 && !mbar_wait_bounded(bar(L::B_EMPTY + slot), (use - 1) & 1, abort, lim)) {
+          if (use > 0 && !waitb(bar(L::B_EMPTY + slot), (use - 1) & 1)) {
             ok = false;
             break;
           }
@@ -260,110 +342,140 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // step) is neither armed nor issued, so the MMA lane's bounded wait
           // for that slot runs out and the whole abort path runs
           if (p.test_stall && ld == 1) continue;
-          mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::TILE);
-          for (int hh = 0; hh < L::NHALF; ++hh)
-            tma_load_2d(kv_smem + slot * L::TILE + hh * L::HALF, (i & 1) ? &tm_v : &tm_k,
-                        bar(L::B_FULL + slot), it.g * D + hh * 64, kt * BN);
+          if (leader) mbar_arrive_expect_tx(bar(L::B_FULL + slot), (PAIR ? 2 : 1) * L::KVSLOT);
+          if constexpr (PAIR) {
+            if (!(i & 1)) {
+              // K: keys [64 r, 64 r + 64) of the key tile, all D columns
+              for (int hh = 0; hh < L::NHALF; ++hh)
+                tma_load_2d_pair(kv_smem + slot * L::KVSLOT + hh * L::KSPAN, &tm_k, lbar(L::B_FULL + slot),
+                                 it.g * D + hh * 64, kt * BN + static_cast<int>(rank) * 64);
+            } else {
+              // V: columns [64 r, 64 r + 64) of all 128 keys
+              tma_load_2d_pair(kv_smem + slot * L::KVSLOT, &tm_v, lbar(L::B_FULL + slot),
+                               it.g * D + static_cast<int>(rank) * 64, kt * BN);
+            }
+          } else {
+            for (int hh = 0; hh < L::NHALF; ++hh)
+              tma_load_2d(kv_smem + slot * L::TILE + hh * L::HALF, (i & 1) ? &tm_v : &tm_k,
+                          bar(L::B_FULL + slot), it.g * D + hh * 64, kt * BN);
+          }
         }
       }
       if (*abort) {
         // let the loads already in flight land before the CTA retires
-        if (nonempty > 0) wait_drain(bar(L::B_Q), (nonempty - 1) & 1, 20000000ull);
-        const uint32_t from = ld > static_cast<uint32_t>(NS) ? ld - NS : 0;
-        for (uint32_t i = from; i < ld; ++i)
-          wait_drain(bar(L::B_FULL + i % NS), (i / NS) & 1, 20000000ull);
+        if (leader) {
+          if (nonempty > 0) wait_drain(bar(L::B_Q), (nonempty - 1) & 1, 20000000ull);
+          const uint32_t from = ld > static_cast<uint32_t>(NS) ? ld - NS : 0;
+          for (uint32_t i = from; i < ld; ++i)
+            wait_drain(bar(L::B_FULL + i % NS), (i / NS) & 1, 20000000ull);
+        } else {
+          // rank 1's loads count on rank 0's barriers, which it cannot
+          // wait on: give them a bounded time to land
+          const uint64_t until = globaltimer_ns() + 200000ull;
+          while (globaltimer_ns() < until) {
+          }
+        }
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);
+    // (in a pair only rank 0 issues, for both CTAs)
+    if (lane == 0 && leader) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(PAIR ? 2 * BM : BM, D, 1);
       auto issue_qk = [=](int t, int slot) {
         const uint32_t d_tmem = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::HALF + (kk & 3) * 32;
-          mma_ss(d_tmem, smem_desc_sw128(q_smem + t * L::TILE + off, 16, 1024),
-                 smem_desc_sw128(kv_smem + slot * L::TILE + off, 16, 1024), IDESC_QK, kk > 0);
+          const uint32_t qoff = (kk >> 2) * L::HALF + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * L::KSPAN + (kk & 3) * 32;
+          const uint64_t a = smem_desc_sw128(q_smem + t * L::TILE + qoff, 16, 1024);
+          const uint64_t b = smem_desc_sw128(kv_smem + slot * L::KVSLOT + koff, 16, 1024);
+          if constexpr (PAIR) mma_ss_pair(d_tmem, a, b, IDESC_QK, kk > 0);
+          else mma_ss(d_tmem, a, b, IDESC_QK, kk > 0);
         }
       };
       auto issue_pv = [=](int t, int slot, bool first) {
         const uint32_t d_tmem = tmem + 256 + t * 128;
         const uint32_t a_tmem = tmem + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(d_tmem, a_tmem + kk * 8,
-                 smem_desc_sw128(kv_smem + slot * L::TILE + kk * 16 * 128, L::HALF, 1024), IDESC_PV,
-                 (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // V MN-major: 16 keys per MMA; the two 64-column spans of V are
+          // L::HALF apart (in a pair each CTA holds one of them)
+          const uint64_t b = smem_desc_sw128(kv_smem + slot * L::KVSLOT + kk * 16 * 128, L::HALF, 1024);
+          if constexpr (PAIR) mma_ts_pair(d_tmem, a_tmem + kk * 8, b, IDESC_PV, (first && kk == 0) ? 0u : 1u);
+          else mma_ts(d_tmem, a_tmem + kk * 8, b, IDESC_PV, (first && kk == 0) ? 0u : 1u);
+        }
       };
       uint32_t ld = 0, nonempty = 0, step = 0;
       bool ok = true;
       uint32_t qpos = 0;
       while (ok) {
         const int qs = qpos % IQ;
-        if (!mbar_wait_bounded(bar(L::B_IF + qs), (qpos / IQ) & 1, abort, lim)) {
+        if (!waitb(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
           ok = false;
           break;
         }
         const int item = iq[qs];
-        mbar_arrive(bar(L::B_IE + qs));
+        if constexpr (PAIR) mbar_arrive_cluster(lbar(L::B_IE + qs));
+        else mbar_arrive(bar(L::B_IE + qs));
         ++qpos;
         if (item >= p.n_items) break;
         const Item it = decode(p, item);
         const int n = it.n;
         if (n == 0) continue;
-        ok = mbar_wait_bounded(bar(L::B_Q), nonempty & 1, abort, lim) &&
-             mbar_wait_bounded(bar(L::B_FULL + ld % NS), (ld / NS) & 1, abort, lim);
+        ok = waitb(bar(L::B_Q), nonempty & 1) &&
+             waitb(bar(L::B_FULL + ld % NS), (ld / NS) & 1);
         if (!ok) break;
         tc_fence_after();
         issue_qk(0, ld % NS);
-        mma_commit(bar(L::B_S + 0));
+        commit(bar(L::B_S + 0));
         issue_qk(1, ld % NS);
-        mma_commit(bar(L::B_S + 1));
-        mma_commit(bar(L::B_EMPTY + ld % NS));
-        if (n == 1) mma_commit(bar(L::B_QE));
+        commit(bar(L::B_S + 1));
+        commit(bar(L::B_EMPTY + ld % NS));
+        if (n == 1) commit(bar(L::B_QE));
         ++ld;
         for (int j = 0; j < n; ++j, ++step) {
           const uint32_t vpos = ld, kpos = ld + 1;
           const bool more = j + 1 < n;
-          if (!mbar_wait_bounded(bar(L::B_FULL + vpos % NS), (vpos / NS) & 1, abort, lim) ||
-              !mbar_wait_bounded(bar(L::B_P + 0), step & 1, abort, lim)) {
+          if (!waitb(bar(L::B_FULL + vpos % NS), (vpos / NS) & 1) ||
+              !waitb(bar(L::B_P + 0), step & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_pv(0, vpos % NS, j == 0);
-          if (!more) mma_commit(bar(L::B_O + 0));
+          if (!more) commit(bar(L::B_O + 0));
           if (more) {
-            if (!mbar_wait_bounded(bar(L::B_FULL + kpos % NS), (kpos / NS) & 1, abort, lim)) {
+            if (!waitb(bar(L::B_FULL + kpos % NS), (kpos / NS) & 1)) {
               ok = false;
               break;
             }
             tc_fence_after();
             issue_qk(0, kpos % NS);
-            mma_commit(bar(L::B_S + 0));
+            commit(bar(L::B_S + 0));
           }
-          if (!mbar_wait_bounded(bar(L::B_P + 1), step & 1, abort, lim)) {
+          if (!waitb(bar(L::B_P + 1), step & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_pv(1, vpos % NS, j == 0);
-          mma_commit(bar(L::B_EMPTY + vpos % NS));
-          if (!more) mma_commit(bar(L::B_O + 1));
+          commit(bar(L::B_EMPTY + vpos % NS));
+          if (!more) commit(bar(L::B_O + 1));
           if (more) {
             issue_qk(1, kpos % NS);
-            mma_commit(bar(L::B_S + 1));
-            mma_commit(bar(L::B_EMPTY + kpos % NS));
-            if (j + 2 == n) mma_commit(bar(L::B_QE));
+            commit(bar(L::B_S + 1));
+            commit(bar(L::B_EMPTY + kpos % NS));
+            if (j + 2 == n) commit(bar(L::B_QE));
           }
           ld += more ? 2 : 1;
         }
         ++nonempty;
       }
       // every MMA this thread issued completes before tensor memory is freed
-      mma_commit(bar(L::B_DRAIN));
+      if constexpr (PAIR) mma_commit_pair_mc(bar(L::B_DRAIN), 1);
+      else mma_commit(bar(L::B_DRAIN));
       wait_drain(bar(L::B_DRAIN), 0, 20000000ull);
     }
     __syncwarp();
@@ -374,13 +486,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t qpos = 0;
     while (ok) {
       const int qs = qpos % IQ;
-      if (!wait_all(bar(L::B_IF + qs), (qpos / IQ) & 1, abort, lim)) {
+      if (!waitw(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
         ok = false;
         break;
       }
       const int item = iq[qs];
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_IE + qs));
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(lbar(L::B_IE + qs));
+        else mbar_arrive(bar(L::B_IE + qs));
+      }
       ++qpos;
       if (item >= p.n_items) break;
       const Item it = decode(p, item);
@@ -431,17 +546,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t qpos = 0;
     while (ok) {
       const int qs = qpos % IQ;
-      if (!wait_all(bar(L::B_IF + qs), (qpos / IQ) & 1, abort, lim)) {
+      if (!waitw(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
         ok = false;
         break;
       }
       const int item = iq[qs];
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_IE + qs));
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(lbar(L::B_IE + qs));
+        else mbar_arrive(bar(L::B_IE + qs));
+      }
       ++qpos;
       if (item >= p.n_items) break;
       const Item it = decode(p, item);
-      const int row = it.qt * 256 + t * BM + wl * 32 + lane;
+      const int row0 = it.qt * ITEM_ROWS + t * TILE_ROWS + static_cast<int>(rank) * BM;   // this CTA's rows of tile t
+      const int row = row0 + wl * 32 + lane;
       const bool live = row < p.sq;
       const size_t obase = (static_cast<size_t>(row) * p.hq + it.h) * D;
       float m_ref = -INFINITY, l = 0.f;
@@ -464,7 +583,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::B_RE + slot));
-        if (!wait_all(bar(L::B_S + t), step & 1, abort, lim)) {
+        if (!waitw(bar(L::B_S + t), step & 1)) {
           ok = false;
           break;
         }
@@ -559,7 +678,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(L::B_P + t));
+        if constexpr (PAIR) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lbar(L::B_P + t));
+        } else {
+          mbar_arrive(bar(L::B_P + t));
+        }
         if (ee_due) {
           // a KV step after the last item's stores were issued: they have read
           // the staging by now, normally without waiting
@@ -571,7 +695,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
       if (it.n > 0) {
-        if (!wait_all(bar(L::B_O + t), nonempty & 1, abort, lim)) {
+        if (!waitw(bar(L::B_O + t), nonempty & 1)) {
           ok = false;
           break;
         }
@@ -589,7 +713,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // epilogue, if that comes first).
         const uint32_t stg = sb + L::ST_OFF + t * L::TILE;
         const int r = wl * 32 + lane;
-        const int y0 = it.qt * 256 + t * BM;
+        const int y0 = row0;
         if (ep > 0) {
           if (ee_due) {
             bulk_wait_read_all();
@@ -666,8 +790,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // a pair's MMAs read and write both CTAs' memory: neither frees its tensor
+  // memory or retires before the other is done
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tmem, 512);
+  if (warp == 9) {
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
+  }
   if (threadIdx.x == 0) {
     if (*abort) atomicCAS(&g_fwd_status, 0u, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
     // every CTA has fetched its last item id once it gets here: the last one
@@ -705,34 +835,70 @@ static unsigned int *next_counter() {
   return base[dev] + (g_launch_seq.fetch_add(1) % SCHED_SLOTS);
 }
 
-template <int D, int NS, int POLY>
+template <int D, int NS, int POLY, bool PAIR>
 static int launch_fwd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                      const CUtensorMap &mo, const FwdParams &p, int grid, cudaStream_t s) {
-  using L = Layout<D, NS>;
+                      const CUtensorMap &mo, FwdParams p, long long items, cudaStream_t s) {
+  using L = Layout<D, NS, PAIR>;
+  auto kern = fwd_kernel<D, NS, POLY, PAIR>;
   static bool configured[kMaxDev] = {};
+  static int max_clusters[kMaxDev] = {};   // co-resident CTA pairs (cluster launch)
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = s;
+  int pairs = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!configured[dev]) {
-      if (cudaFuncSetAttribute(fwd_kernel<D, NS, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               L::ALLOC) != cudaSuccess)
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) !=
+          cudaSuccess)
         return ATTN_ERR_CUDA;
+      if constexpr (PAIR) {
+        cfg.gridDim = dim3(2 * 76);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&max_clusters[dev], kern, &cfg) != cudaSuccess ||
+            max_clusters[dev] < 1)
+          return ATTN_ERR_CUDA;
+      }
       configured[dev] = true;
     }
+    pairs = max_clusters[dev];
   }
-  fwd_kernel<D, NS, POLY><<<grid, NTHREADS, L::ALLOC, s>>>(mq, mk, mv, mo, p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  if constexpr (!PAIR) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    const int grid = static_cast<int>(items < sms ? items : sms);
+    kern<<<grid, NTHREADS, L::ALLOC, s>>>(mq, mk, mv, mo, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  } else {
+    // one persistent CTA pair per co-resident cluster slot
+    const int np = static_cast<int>(items < pairs ? items : pairs);
+    cfg.gridDim = dim3(2 * np);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, p) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
 }
 
 int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int hq, int hk, int d,
                float scale, const attn_tiles_t *tiles, void *out, int out_dtype, float *lse,
                cudaStream_t stream) {
+  // metadata of 512-row query tiles selects the CTA-pair kernel (d = 128)
+  const bool pair = tiles->tile_q == 2 * ATTN_FWD_TILE_Q;
   CUtensorMap mq, mk, mv, mo;
   int rc;
   if ((rc = make_tma_2d(&mq, q, static_cast<uint64_t>(hq) * d, sq)) != ATTN_OK) return rc;
-  if ((rc = make_tma_2d(&mk, k, static_cast<uint64_t>(hk) * d, sk)) != ATTN_OK) return rc;
+  // a pair's CTA loads 64 keys of each K tile
+  if ((rc = make_tma_2d(&mk, k, static_cast<uint64_t>(hk) * d, sk, pair ? 64 : 128)) != ATTN_OK) return rc;
   if ((rc = make_tma_2d(&mv, v, static_cast<uint64_t>(hk) * d, sk)) != ATTN_OK) return rc;
   FwdParams p;
   p.row_ptr = tiles->row_ptr;
@@ -762,9 +928,6 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   if (items == 0) return ATTN_OK;
   if (items >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   p.n_items = static_cast<int>(items);
-  const int sms = device_sm_count();
-  if (sms <= 0) return ATTN_ERR_CUDA;
-  const int grid = static_cast<int>(items < sms ? items : sms);
   p.counter = next_counter();
   if (!p.counter) return ATTN_ERR_CUDA;
   p.meta_status = reinterpret_cast<const long long *>(tiles->totals + 3);
@@ -774,15 +937,16 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   // own abort path without faulting or hanging the GPU
   const char *stall = std::getenv("ATTN_TEST_STALL_FWD");
   p.test_stall = stall && stall[0] == '1';
+  if (pair) return launch_fwd<128, 6, 0, true>(mq, mk, mv, mo, p, items, stream);
   const int poly = g_exp2_poly;
   if (d == 128) {
-    if (poly == 4) return launch_fwd<128, 3, 4>(mq, mk, mv, mo, p, grid, stream);
-    if (poly == 8) return launch_fwd<128, 3, 8>(mq, mk, mv, mo, p, grid, stream);
-    return launch_fwd<128, 3, 0>(mq, mk, mv, mo, p, grid, stream);
+    if (poly == 4) return launch_fwd<128, 3, 4, false>(mq, mk, mv, mo, p, items, stream);
+    if (poly == 8) return launch_fwd<128, 3, 8, false>(mq, mk, mv, mo, p, items, stream);
+    return launch_fwd<128, 3, 0, false>(mq, mk, mv, mo, p, items, stream);
   }
-  if (poly == 4) return launch_fwd<64, 8, 4>(mq, mk, mv, mo, p, grid, stream);
-  if (poly == 8) return launch_fwd<64, 8, 8>(mq, mk, mv, mo, p, grid, stream);
-  return launch_fwd<64, 8, 0>(mq, mk, mv, mo, p, grid, stream);
+  if (poly == 4) return launch_fwd<64, 8, 4, false>(mq, mk, mv, mo, p, items, stream);
+  if (poly == 8) return launch_fwd<64, 8, 8, false>(mq, mk, mv, mo, p, items, stream);
+  return launch_fwd<64, 8, 0, false>(mq, mk, mv, mo, p, items, stream);
 }
 
 int fwd_status_take(unsigned int *status) {

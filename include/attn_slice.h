@@ -82,9 +82,13 @@ typedef struct CUstream_st *attn_stream_t;
 #define ATTN_DTYPE_BF16 0
 #define ATTN_DTYPE_F32  1
 
-/* Forward kernel tile shape: 256 query rows (two 128-row MMA tiles) by 128
- * keys.  attn_fwd requires tiles built with exactly this shape. */
+/* Forward kernel tile shapes: 256 query rows (two 128-row MMA tiles) by 128
+ * keys for the single-CTA kernel; 512 query rows by 128 keys (head dim 128)
+ * selects the CTA-pair kernel, in which two CTAs of a cluster share each
+ * M = 256 MMA and each loads half of every K/V tile (FlashAttention-4 page,
+ * 2-CTA MMA).  attn_fwd requires tiles built with one of these shapes. */
 #define ATTN_FWD_TILE_Q 256
+#define ATTN_FWD_PAIR_TILE_Q 512
 #define ATTN_FWD_TILE_K 128
 #define ATTN_MERGE_MAX_PARTS 16
 
@@ -209,7 +213,10 @@ int attn_slices_from_block_grid(const uint8_t *h_grid, int nbq, int nbk, int blo
  *   d           head dim, 64 or 128
  *   scale       softmax scale (> 0, finite), applied to q . k
  *   tiles       metadata from attn_build_tiles with tile shape
- *               ATTN_FWD_TILE_Q x ATTN_FWD_TILE_K
+ *               ATTN_FWD_TILE_Q x ATTN_FWD_TILE_K, or (d = 128 only)
+ *               ATTN_FWD_PAIR_TILE_Q x ATTN_FWD_TILE_K for the CTA-pair
+ *               kernel (clusters of two CTAs; the attn_set_exp2_poly mode
+ *               does not apply to it: every exponential stays on MUFU)
  *   out         [sq, hq, d] of out_dtype (ATTN_DTYPE_BF16 or _F32)
  *   lse         [hq, sq] f32: ln sum exp(scale q.k) over valid keys
  * A query row with no valid key gets O = 0 and lse = -inf.  q, k and v must
