@@ -135,21 +135,32 @@ struct Item {
   int qt, h, g, e0, n;
 };
 
-// Work item -> (query tile, head).  Items run KV-head-group-major: all items
-// of KV head 0's group first (query tiles in longest-processing-time order,
-// for each query tile the group's query heads in turn), then group 1, and so
-// on.  The CTAs working at any moment then sweep the keys and values of one
-// or two KV heads (67 MB at S = 131072, d = 128), which stay in L2, instead
-// of those of every head; the order within a group, and the shortest items
-// coming last overall, keep the balance of the longest-processing-time order.
-__device__ __forceinline__ Item decode(const FwdParams &p, int item) {
+// Work item -> (query tile, head), in one of two orders.
+//   query-tile-major: query tiles in longest-processing-time order, each
+//     with all of its heads in turn -- the plain LPT order;
+//   KV-group-major: all items of KV head 0's group first (query tiles in LPT
+//     order, for each the group's query heads in turn), then group 1, ...
+// In the second order the CTAs working at any moment sweep the keys and
+// values of one or two KV heads, which stay in L2 (67 MB at S = 131072,
+// d = 128), instead of those of every head: on the long GQA causal problem
+// DRAM reads fall from 102.6 GB to 3.1 GB per launch.  But the last group's
+// longest item starts when (H_k - 1) / H_k of the work is handed out, so it
+// only keeps the LPT balance when the longest item times H_k fits in one
+// CTA's share of the work; group_major is chosen per launch by that test.
+__device__ __forceinline__ Item decode(const FwdParams &p, int item, bool group_major) {
   Item it;
-  const int G = p.hq / p.hk;             // query heads per KV head
-  const int per_group = p.n_items / p.hk;
-  it.g = item / per_group;
-  const int r = item - it.g * per_group;
-  it.qt = __ldg(p.sched + r / G);
-  it.h = it.g * G + r % G;
+  if (group_major) {
+    const int G = p.hq / p.hk;             // query heads per KV head
+    const int per_group = p.n_items / p.hk;
+    it.g = item / per_group;
+    const int r = item - it.g * per_group;
+    it.qt = __ldg(p.sched + r / G);
+    it.h = it.g * G + r % G;
+  } else {
+    it.qt = __ldg(p.sched + item / p.hq);
+    it.h = item % p.hq;
+    it.g = it.h / (p.hq / p.hk);
+  }
   it.e0 = __ldg(p.row_ptr + it.qt);
   it.n = __ldg(p.row_ptr + it.qt + 1) - it.e0;
   return it;
@@ -187,6 +198,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
   volatile int *meta_bad = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 8);
+  volatile int *order = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 12);
   Rec *recs = reinterpret_cast<Rec *>(smem + L::REC_OFF);
   volatile int *iq = reinterpret_cast<volatile int *>(smem + L::IQ_OFF);
 
@@ -251,6 +263,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const long long ms = *p.meta_status;
     *meta_bad = ms != ATTN_OK;
     if (ms != ATTN_OK) atomicCAS(&g_fwd_status, 0u, static_cast<unsigned>(ms));
+    // item order (see decode): KV-group-major when the longest item (the
+    // first query tile of the LPT order) times H_k is at most one CTA's (or
+    // pair's) share of all entries
+    *order = 0;
+    if (ms == ATTN_OK) {
+      const int nq = p.n_items / p.hq;
+      const int q0 = __ldg(p.sched);
+      const long long longest = __ldg(p.row_ptr + q0 + 1) - __ldg(p.row_ptr + q0);
+      const long long total = __ldg(p.row_ptr + nq);
+      const long long units = PAIR ? gridDim.x / 2 : gridDim.x;
+      *order = longest * p.hk * units <= total * p.hq;
+    }
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -308,7 +332,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         ++qpos;
         if (item >= p.n_items) break;
-        const Item it = decode(p, item);
+        const Item it = decode(p, item, *order != 0);
         if (it.n == 0) continue;
         if (nonempty > 0 && !waitb(bar(L::B_QE), (nonempty - 1) & 1)) {
           ok = false;
@@ -421,7 +445,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         else mbar_arrive(bar(L::B_IE + qs));
         ++qpos;
         if (item >= p.n_items) break;
-        const Item it = decode(p, item);
+        const Item it = decode(p, item, *order != 0);
         const int n = it.n;
         if (n == 0) continue;
         ok = waitb(bar(L::B_Q), nonempty & 1) &&
@@ -498,7 +522,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       ++qpos;
       if (item >= p.n_items) break;
-      const Item it = decode(p, item);
+      const Item it = decode(p, item, *order != 0);
       for (int base = 0; ok && base < it.n; base += 32) {
         const int j = base + lane, cnt = min(32, it.n - base);
         Rec r;
@@ -558,7 +582,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       ++qpos;
       if (item >= p.n_items) break;
-      const Item it = decode(p, item);
+      const Item it = decode(p, item, *order != 0);
       const int row0 = it.qt * ITEM_ROWS + t * TILE_ROWS + static_cast<int>(rank) * BM;   // this CTA's rows of tile t
       const int row = row0 + wl * 32 + lane;
       const bool live = row < p.sq;
