@@ -211,15 +211,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // load completions of both CTAs count there)
   const uint32_t lbar0 = PAIR ? mapa_shared(sb + L::BAR_OFF, 0) : sb + L::BAR_OFF;
   auto lbar = [&](int i) -> uint32_t { return lbar0 + 8u * i; };
-  // waits on barriers the other CTA of a pair may complete acquire at
-  // cluster scope
-  auto waitb = [&](uint32_t b, uint32_t par) -> bool {
+  // Waits.  waitb / waitw: barriers completed by this CTA's threads or by
+  // asynchronous operations (tensor-core commits, TMA byte counts), also
+  // when rank 0 of a pair issued them.  waitc / waitwc: barriers that
+  // threads of the other CTA of a pair arrive on, carrying their earlier
+  // writes (P in tensor memory, item ids, queue reads): those acquire at
+  // cluster scope.
+  auto waitb = [&](uint32_t b, uint32_t par) -> bool { return mbar_wait_bounded(b, par, abort, lim); };
+  auto waitw = [&](uint32_t b, uint32_t par) -> bool { return wait_all(b, par, abort, lim); };
+  auto waitc = [&](uint32_t b, uint32_t par) -> bool {
     if constexpr (PAIR) return mbar_wait_bounded_cl(b, par, abort, lim);
     else return mbar_wait_bounded(b, par, abort, lim);
   };
-  auto waitw = [&](uint32_t b, uint32_t par) -> bool {
+  auto waitwc = [&](uint32_t b, uint32_t par) -> bool {
     if constexpr (PAIR) return wait_all_cl(b, par, abort, lim);
     else return wait_all(b, par, abort, lim);
+  };
+  // arrival on rank 0's barrier i: local for rank 0's own threads, remote
+  // with cluster-scope release for rank 1's
+  auto arrive0 = [&](int i) {
+    if (PAIR && !leader) mbar_arrive_cluster(lbar(i));
+    else mbar_arrive(bar(i));
   };
   // rank 0's tensor-core commits arrive on both CTAs of a pair
   auto commit = [&](uint32_t b) {
@@ -309,7 +321,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int qs = qpos % IQ;
         int item;
         if (leader) {
-          if (qpos >= IQ && !waitb(bar(L::B_IE + qs), (qpos / IQ - 1) & 1)) {
+          if (qpos >= IQ && !waitc(bar(L::B_IE + qs), (qpos / IQ - 1) & 1)) {
             ok = false;
             break;
           }
@@ -323,12 +335,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mbar_arrive(bar(L::B_IF + qs));
         } else {
           // rank 1 of a pair: the item rank 0 published
-          if (!waitb(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
+          if (!waitc(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
             ok = false;
             break;
           }
           item = iq[qs];
-          mbar_arrive_cluster(lbar(L::B_IE + qs));
+          arrive0(L::B_IE + qs);
         }
         ++qpos;
         if (item >= p.n_items) break;
@@ -441,8 +453,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         }
         const int item = iq[qs];
-        if constexpr (PAIR) mbar_arrive_cluster(lbar(L::B_IE + qs));
-        else mbar_arrive(bar(L::B_IE + qs));
+        arrive0(L::B_IE + qs);
         ++qpos;
         if (item >= p.n_items) break;
         const Item it = decode(p, item, *order != 0);
@@ -463,7 +474,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t vpos = ld, kpos = ld + 1;
           const bool more = j + 1 < n;
           if (!waitb(bar(L::B_FULL + vpos % NS), (vpos / NS) & 1) ||
-              !waitb(bar(L::B_P + 0), step & 1)) {
+              !waitc(bar(L::B_P + 0), step & 1)) {
             ok = false;
             break;
           }
@@ -479,7 +490,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             issue_qk(0, kpos % NS);
             commit(bar(L::B_S + 0));
           }
-          if (!waitb(bar(L::B_P + 1), step & 1)) {
+          if (!waitc(bar(L::B_P + 1), step & 1)) {
             ok = false;
             break;
           }
@@ -510,16 +521,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t qpos = 0;
     while (ok) {
       const int qs = qpos % IQ;
-      if (!waitw(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
+      if (!waitwc(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
         ok = false;
         break;
       }
       const int item = iq[qs];
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR) mbar_arrive_cluster(lbar(L::B_IE + qs));
-        else mbar_arrive(bar(L::B_IE + qs));
-      }
+      if (lane == 0) arrive0(L::B_IE + qs);
       ++qpos;
       if (item >= p.n_items) break;
       const Item it = decode(p, item, *order != 0);
@@ -570,16 +578,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t qpos = 0;
     while (ok) {
       const int qs = qpos % IQ;
-      if (!waitw(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
+      if (!waitwc(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
         ok = false;
         break;
       }
       const int item = iq[qs];
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR) mbar_arrive_cluster(lbar(L::B_IE + qs));
-        else mbar_arrive(bar(L::B_IE + qs));
-      }
+      if (lane == 0) arrive0(L::B_IE + qs);
       ++qpos;
       if (item >= p.n_items) break;
       const Item it = decode(p, item, *order != 0);
@@ -704,7 +709,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         if constexpr (PAIR) {
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(lbar(L::B_P + t));
+          if (lane == 0) arrive0(L::B_P + t);
         } else {
           mbar_arrive(bar(L::B_P + t));
         }
