@@ -147,22 +147,42 @@ struct Item {
 // longest item starts when (H_k - 1) / H_k of the work is handed out, so it
 // only keeps the LPT balance when the longest item times H_k fits in one
 // CTA's share of the work; group_major is chosen per launch by that test.
-__device__ __forceinline__ Item decode(const FwdParams &p, int item, bool group_major) {
-  Item it;
+// Head, KV group and LPT position (index into sched) of a work item.
+__device__ __forceinline__ int item_head(const FwdParams &p, int item, bool group_major, int &h, int &g) {
   if (group_major) {
     const int G = p.hq / p.hk;             // query heads per KV head
     const int per_group = p.n_items / p.hk;
-    it.g = item / per_group;
-    const int r = item - it.g * per_group;
-    it.qt = __ldg(p.sched + r / G);
-    it.h = it.g * G + r % G;
-  } else {
-    it.qt = __ldg(p.sched + item / p.hq);
-    it.h = item % p.hq;
-    it.g = it.h / (p.hq / p.hk);
+    g = item / per_group;
+    const int r = item - g * per_group;
+    h = g * G + r % G;
+    return r / G;
   }
+  h = item % p.hq;
+  g = h / (p.hq / p.hk);
+  return item / p.hq;
+}
+__device__ __forceinline__ Item decode(const FwdParams &p, int item, bool group_major) {
+  Item it;
+  it.qt = __ldg(p.sched + item_head(p, item, group_major, it.h, it.g));
   it.e0 = __ldg(p.row_ptr + it.qt);
   it.n = __ldg(p.row_ptr + it.qt + 1) - it.e0;
+  return it;
+}
+// The producer publishes each item decoded: queue slot qs holds {item, query
+// tile, first entry, entry count}, so the other roles start from shared
+// memory instead of repeating the dependent sched / row_ptr loads.
+struct QItem {
+  int item, qt, e0, n;
+};
+__device__ __forceinline__ QItem read_slot(volatile int *iq, int qs) {
+  return QItem{iq[4 * qs], iq[4 * qs + 1], iq[4 * qs + 2], iq[4 * qs + 3]};
+}
+__device__ __forceinline__ Item from_slot(const FwdParams &p, const QItem &q, bool group_major) {
+  Item it;
+  item_head(p, q.item, group_major, it.h, it.g);
+  it.qt = q.qt;
+  it.e0 = q.e0;
+  it.n = q.n;
   return it;
 }
 
@@ -326,10 +346,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             break;
           }
           item = static_cast<int>(atomicAdd(p.counter, 1u));
-          iq[qs] = item;
+          Item d{0, 0, 0, 0, 0};
+          if (item < p.n_items) d = decode(p, item, *order != 0);
+          const int w[4] = {item, d.qt, d.e0, d.n};
+          for (int k = 0; k < 4; ++k) iq[4 * qs + k] = w[k];
           if constexpr (PAIR) {
             // publish to rank 1's queue as well
-            st_shared_cluster_u32(mapa_shared(sb + L::IQ_OFF + 4u * qs, 1), static_cast<uint32_t>(item));
+            for (int k = 0; k < 4; ++k)
+              st_shared_cluster_u32(mapa_shared(sb + L::IQ_OFF + 16u * qs + 4u * k, 1), static_cast<uint32_t>(w[k]));
             mbar_arrive_cluster(mapa_shared(bar(L::B_IF + qs), 1));
           }
           mbar_arrive(bar(L::B_IF + qs));
@@ -339,12 +363,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
-          item = iq[qs];
-          arrive0(L::B_IE + qs);
+          item = iq[4 * qs];
         }
+        const QItem qi = read_slot(iq, qs);
+        if (PAIR && !leader) arrive0(L::B_IE + qs);
         ++qpos;
         if (item >= p.n_items) break;
-        const Item it = decode(p, item, *order != 0);
+        const Item it = from_slot(p, qi, *order != 0);
         if (it.n == 0) continue;
         if (nonempty > 0 && !waitb(bar(L::B_QE), (nonempty - 1) & 1)) {
           ok = false;
@@ -452,11 +477,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           ok = false;
           break;
         }
-        const int item = iq[qs];
+        const QItem qi = read_slot(iq, qs);
+        const int item = qi.item;
         arrive0(L::B_IE + qs);
         ++qpos;
         if (item >= p.n_items) break;
-        const Item it = decode(p, item, *order != 0);
+        const Item it = from_slot(p, qi, *order != 0);
         const int n = it.n;
         if (n == 0) continue;
         ok = waitb(bar(L::B_Q), nonempty & 1) &&
@@ -525,12 +551,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = false;
         break;
       }
-      const int item = iq[qs];
+      const QItem qi = read_slot(iq, qs);
+      const int item = qi.item;
       __syncwarp();
       if (lane == 0) arrive0(L::B_IE + qs);
       ++qpos;
       if (item >= p.n_items) break;
-      const Item it = decode(p, item, *order != 0);
+      const Item it = from_slot(p, qi, *order != 0);
       for (int base = 0; ok && base < it.n; base += 32) {
         const int j = base + lane, cnt = min(32, it.n - base);
         Rec r;
@@ -582,12 +609,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = false;
         break;
       }
-      const int item = iq[qs];
+      const QItem qi = read_slot(iq, qs);
+      const int item = qi.item;
       __syncwarp();
       if (lane == 0) arrive0(L::B_IE + qs);
       ++qpos;
       if (item >= p.n_items) break;
-      const Item it = decode(p, item, *order != 0);
+      const Item it = from_slot(p, qi, *order != 0);
       const int row0 = it.qt * ITEM_ROWS + t * TILE_ROWS + static_cast<int>(rank) * BM;   // this CTA's rows of tile t
       const int row = row0 + wl * 32 + lane;
       const bool live = row < p.sq;
@@ -756,22 +784,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
 #pragma unroll 1
         for (int hh = 0; hh < L::NHALF; ++hh) {
+          // both 32-column loads of this 64-column half in flight, one wait
+          uint32_t x[64];
+          if (it.n > 0) {
+            tmem_ld32(tO + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+            tmem_ld32(tO + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 64; ++k) asm volatile("" : "+r"(x[k]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) x[k] = 0u;
+          }
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t x[32];
-            if (it.n > 0) {
-              tmem_ld32_wait(tO + hh * 64 + c2 * 32, x);
-            } else {
-#pragma unroll
-              for (int k = 0; k < 32; ++k) x[k] = 0u;
-            }
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
+              const uint32_t *y = x + 32 * c2 + 8 * q4;
               uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(x[8 * q4 + 0]) * inv, __uint_as_float(x[8 * q4 + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(x[8 * q4 + 2]) * inv, __uint_as_float(x[8 * q4 + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(x[8 * q4 + 4]) * inv, __uint_as_float(x[8 * q4 + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(x[8 * q4 + 6]) * inv, __uint_as_float(x[8 * q4 + 7]) * inv);
+              v.x = pack_bf16x2(__uint_as_float(y[0]) * inv, __uint_as_float(y[1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(y[2]) * inv, __uint_as_float(y[3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(y[4]) * inv, __uint_as_float(y[5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(y[6]) * inv, __uint_as_float(y[7]) * inv);
               st_shared_v4(stg + hh * L::HALF + r * 128 + (((c2 * 4 + q4) ^ (r & 7)) << 4), v);
             }
           }
