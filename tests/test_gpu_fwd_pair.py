@@ -159,3 +159,59 @@ def test_pair_tiles_need_head_dim_128():
     with pytest.raises(AttnError) as e:
         attn_fwd(q, q, q, t, 0.125)
     assert e.value.code == B.ATTN_ERR_UNSUPPORTED
+
+
+def test_kv_split_partials_merged():
+    # the pair kernel writing f32 partials of a 4-way KV split of the
+    # quarter-length GQA causal problem, merged by attn_merge, against the
+    # oracle of the whole problem (the chunk-c partial: the causal diagonal
+    # block of chunk c and the full block of every later row against it)
+    from block_sparse_attention_slice_gb300 import attn_merge
+    w = W.gqa_causal_32k()
+    q, k, v, qd, kd, vd = _qkv(w)
+    c = w.S // 4
+    parts = []
+    for i in range(4):
+        rows = [(i * c, (i + 1) * c, i * c, (i + 1) * c, W.CAUSAL)]
+        if (i + 1) * c < w.S:
+            rows.append(((i + 1) * c, w.S, i * c, (i + 1) * c, W.FULL))
+        t = attn_build_tiles(np.asarray(rows, np.int32), w.S, w.S, TQ, 128)
+        parts.append(attn_fwd(qd, kd, vd, t, w.scale, out_dtype=torch.float32))
+    mo, ml = attn_merge([x[0] for x in parts], [x[1] for x in parts], out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert B.attn_last_device_error() == 0
+    rows = rows_per_head(w, n=256, extra=[0, 511, 512, w.S - 1] + [i * c + o for i in range(4) for o in (-1, 0)])
+    compare(mo, ml, run_oracle(q, k, v, w.scale, mask_fn(w), rows=rows))
+
+
+def test_pair_abort_path_ends_with_timeout(monkeypatch):
+    # the pair's abort path, driven like the single-CTA kernel's: with
+    # ATTN_TEST_STALL_FWD=1 both CTAs of every pair leave their second K/V
+    # load unissued, so rank 0's bounded wait for that slot runs out; both
+    # CTAs leave their waits, rank 0 waits for its loads and MMAs, rank 1
+    # gives its loads a bounded time to land, and the pair meets at its
+    # closing cluster barrier before freeing tensor memory.  Afterwards the
+    # forward is bit-identical to a run made before.
+    from block_sparse_attention_slice_gb300 import attn_set_wait_limit_ns
+    S, H, Hk = 8192, 4, 2
+    rng = np.random.default_rng(8)
+    mk = lambda h: torch.from_numpy(rng.standard_normal((S, h, 128), dtype=np.float32)).to(torch.bfloat16).cuda()
+    q, k, v = mk(H), mk(Hk), mk(Hk)
+    t = attn_build_tiles(np.array([[0, S, 0, S, 1]], np.int32), S, S, TQ, 128)
+    ref_o, ref_l = attn_fwd(q, k, v, t, 0.088)
+    torch.cuda.synchronize()
+    assert B.attn_last_device_error() == 0
+    attn_set_wait_limit_ns(50_000_000)
+    monkeypatch.setenv("ATTN_TEST_STALL_FWD", "1")
+    try:
+        attn_fwd(q, k, v, t, 0.088)
+        rc = B.attn_last_device_error()
+    finally:
+        monkeypatch.delenv("ATTN_TEST_STALL_FWD")
+        attn_set_wait_limit_ns(4_000_000_000)
+    assert rc == B.ATTN_ERR_TIMEOUT
+    o2, l2 = attn_fwd(q, k, v, t, 0.088)
+    torch.cuda.synchronize()
+    assert B.attn_last_device_error() == 0
+    assert torch.equal(o2.view(torch.int16), ref_o.view(torch.int16))
+    assert torch.equal(l2.view(torch.int32), ref_l.view(torch.int32))
