@@ -204,17 +204,33 @@ def barrier(ws: int):
         dist.barrier()
 
 
+def code_sha16(src: str) -> str:
+    """First 16 hex digits of the SHA-256 of a source file's code: the text
+    with `//` comments and blank lines removed, so that editing a comment does
+    not disown a profile taken on the same compiled kernel."""
+    lines = []
+    for ln in open(src, encoding="utf-8"):
+        cut = ln.find("//")
+        if cut >= 0 and '"' not in ln[:cut]:
+            ln = ln[:cut]
+        ln = ln.rstrip()
+        if ln:
+            lines.append(ln)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def profile_traffic(kernel: str, workload: str, src: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current source of the kernel; else None."""
+    was taken on the current code of the kernel (its `code_sha256_16` line);
+    else None."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     if not os.path.exists(p):
         return None
-    want = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    want = code_sha16(src)
     got, traffic = None, None
     for ln in open(p):
-        if ln.startswith("source_sha256_16:"):
-            got = ln.split(":", 1)[1].strip()
+        if ln.startswith("code_sha256_16:"):
+            got = ln.split(":", 1)[1].split()[0]
         if ln.startswith("dram_bytes_per_launch:"):
             traffic = float(ln.split(":", 1)[1].strip())
     return traffic if got == want else None

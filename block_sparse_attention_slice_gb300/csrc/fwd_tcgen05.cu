@@ -12,11 +12,14 @@
 //
 // Persistent kernel: one CTA per SM takes work items (query tile, head) in
 // longest-processing-time order from a global counter (the producer lane
-// fetches and publishes each item id to the CTA's other roles through a
-// small shared-memory queue), so the CTAs finish together and the next
-// item's Q load and first QK overlap the previous item's epilogue.  A work item is 256
-// query rows of one head (two 128-row MMA tiles, t = 0, 1) against the
-// KV-tile list of that 256-row query tile.  Warp roles (352 threads):
+// fetches each item, decodes it and publishes it to the CTA's other roles
+// through a small shared-memory queue), so the CTAs finish together and the
+// next item's Q load and first QK overlap the previous item's epilogue.  The
+// items run query-tile-major or KV-group-major, chosen per launch (decode()).
+// A work item is 256 query rows of one head (two 128-row MMA tiles, t = 0, 1)
+// against the KV-tile list of that 256-row query tile; the CTA-pair form
+// (PAIR, below) takes 512 rows per item on two CTAs.  Warp roles (352
+// threads):
 //   warps 0-3  softmax of tile 0 (thread = row = tensor-memory lane)
 //   warps 4-7  softmax of tile 1
 //   warp  8    TMA producer: Q of each item, then K_j, V_j through an NS-slot ring
