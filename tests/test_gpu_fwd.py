@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from block_sparse_attention_slice_gb300 import (attn_build_tiles, attn_fwd, attn_merge,
+from block_sparse_attention_slice_gb300 import (attn_build_tiles, attn_fwd, attn_last_device_error, attn_merge,
                                                 attn_slices_from_block_grid)
 from block_sparse_attention_slice_gb300 import workloads as W
 from parity import SAMPLE_ROWS, compare, f64, mask_fn, rows_per_head, run_oracle
@@ -227,3 +227,63 @@ def test_repeat_runs_bit_identical():
     b = attn_fwd(qd, kd, vd, t, w.scale)
     assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
     assert torch.equal(a[1], b[1])
+
+
+def test_concurrent_streams_share_the_library_rings():
+    # forwards and metadata builds of two different problems enqueued on two
+    # streams at once, several times: each launch takes its own work counter
+    # and grid-barrier slot from the library's rings, so the results must be
+    # bit-identical to the same calls made one at a time
+    rng = np.random.default_rng(31)
+    probs = []
+    for S, H, Hk, sl in ((4096, 8, 2, np.array([[0, 4096, 0, 4096, 1]], np.int32)),
+                         (3000, 4, 4, W.random_slices(3000, 3000, 20, seed=77, unit=1, max_len=900))):
+        mk = lambda h: torch.from_numpy(rng.standard_normal((S, h, 128), dtype=np.float32)).to(torch.bfloat16).cuda()
+        probs.append((S, sl, mk(H), mk(Hk), mk(Hk)))
+    ref = []
+    for S, sl, q, k, v in probs:
+        t = attn_build_tiles(sl, S, S)
+        ref.append(attn_fwd(q, k, v, t, 0.088))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(4):
+        outs, keep = [], []
+        for (S, sl, q, k, v), st in zip(probs, streams):
+            with torch.cuda.stream(st):
+                keep.append(attn_build_tiles(sl, S, S))
+                outs.append(attn_fwd(q, k, v, keep[-1], 0.088))
+        torch.cuda.synchronize()
+        for (o, l), (ro, rl) in zip(outs, ref):
+            assert torch.equal(o.view(torch.int16), ro.view(torch.int16))
+            assert torch.equal(l.view(torch.int32), rl.view(torch.int32))
+    assert attn_last_device_error() == 0
+
+
+def test_forward_and_merge_replayed_from_a_cuda_graph():
+    # a serving loop captures attn_fwd (two KV-split partials) and attn_merge
+    # once and replays them; the replays must equal the eager calls bit for
+    # bit (each replay reuses the work counter the capture took, one replay
+    # at a time, as the header requires)
+    w = W.tiny_causal()
+    q, k, v, qd, kd, vd = _qkv(w)
+    tiles = [attn_build_tiles(sl, w.S, w.S) for sl in w.kv_splits]
+    parts = [attn_fwd(qd, kd, vd, t, w.scale, out_dtype=torch.float32) for t in tiles]   # eager (and warm-up)
+    ref_o, ref_l = attn_merge([p[0] for p in parts], [p[1] for p in parts])
+    torch.cuda.synchronize()
+    outs = [(torch.empty_like(p[0]), torch.empty_like(p[1])) for p in parts]
+    mo, ml = torch.empty_like(ref_o), torch.empty_like(ref_l)
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            for t, (o, l) in zip(tiles, outs):
+                attn_fwd(qd, kd, vd, t, w.scale, out=o, lse=l)
+            attn_merge([o for o, _ in outs], [l for _, l in outs], out=mo, lse=ml)
+    for _ in range(3):
+        mo.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(mo.view(torch.int16), ref_o.view(torch.int16))
+        assert torch.equal(ml.view(torch.int32), ref_l.view(torch.int32))
+    assert attn_last_device_error() == 0
