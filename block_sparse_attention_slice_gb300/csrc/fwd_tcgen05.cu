@@ -69,7 +69,7 @@ constexpr int BN = 128;           // keys per KV tile
 constexpr float TAU = 8.0f;       // lazy-rescale threshold, log2 units
 constexpr int NTHREADS = 352;
 constexpr int RING = 16;          // metadata records in flight
-constexpr int IQ = 4;             // queued work-item ids
+constexpr int IQ = 4;             // queued work items (id, query tile, first entry, entry count)
 constexpr int SCHED_SLOTS = 4096; // work counters, one per launch in flight
 
 // Work counters of forward launches: each launch takes the next slot (host
