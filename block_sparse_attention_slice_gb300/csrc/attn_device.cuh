@@ -142,6 +142,21 @@ inline int make_tma_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// 2-D f32 map over a [rows, cols] row-major matrix, 32 x 128 boxes (128-byte
+// rows), no swizzle: used to store rows of zeros from shared memory.
+inline int make_tma_2d_f32(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows) {
+  auto enc = tma_encode_fn();
+  if (!enc) return ATTN_ERR_CUDA;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // Number of SMs of the current device (cached per device), or -1.
 inline int device_sm_count() {
   constexpr int kMax = 64;

@@ -606,6 +606,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t step = 0, rpos = 0, nonempty = 0, ep = 0;
     bool ok = true;
     uint32_t qpos = 0;
+    // f32 output: the tile's bf16 staging buffer is unused, so it is zeroed
+    // once and rows of items with no key tile (O = 0; e.g. the rows before a
+    // KV-split chunk, most of a late chunk's partial) leave as TMA stores of
+    // it, whole 128-byte row segments, instead of one 16-byte store per row
+    const uint32_t zero_buf = sb + L::ST_OFF + t * L::TILE;
+    if (p.out_f32) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int off = (wl * 32 + lane) * 16; off < L::TILE; off += 128 * 16) st_shared_v4(zero_buf + off, z);
+      fence_proxy_async_smem();
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");   // the tile's 128 threads
+    }
     while (ok) {
       const int qs = qpos % IQ;
       if (!waitwc(bar(L::B_IF + qs), (qpos / IQ) & 1)) {
@@ -824,6 +835,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           ee_due = true;
         }
         ++ep;
+      } else if (it.n == 0) {
+        // f32 O of an item with no key tile: zeros, 32 columns x 128 rows per store
+        if (elected && row0 < p.sq) {
+          for (int c = 0; c < D / 32; ++c) tma_store_2d(&tm_o, zero_buf, it.h * D + 32 * c, row0);
+          bulk_commit_group();
+        }
       } else {
         // f32 O (KV-split partials): one thread per row, 16-byte stores
 #pragma unroll 1
@@ -981,12 +998,13 @@ int fwd_launch(const void *q, const void *k, const void *v, int sq, int sk, int 
   p.hq = hq;
   p.hk = hk;
   p.out_f32 = out_dtype == ATTN_DTYPE_F32;
-  // bf16 O is stored by TMA through the same 64 x 128 box format as Q; the
-  // f32 path (partials) keeps one thread per row and needs no map
+  // bf16 O is stored by TMA through the same 64 x 128 box format as Q; f32 O
+  // (partials) keeps one thread per row, and rows of items with no key tile
+  // are zeroed by TMA stores of 32 x 128 f32 boxes
   if (!p.out_f32) {
     if ((rc = make_tma_2d(&mo, out, static_cast<uint64_t>(hq) * d, sq)) != ATTN_OK) return rc;
   } else {
-    mo = mq;
+    if ((rc = make_tma_2d_f32(&mo, out, static_cast<uint64_t>(hq) * d, sq)) != ATTN_OK) return rc;
   }
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_ns = g_wait_ns;
