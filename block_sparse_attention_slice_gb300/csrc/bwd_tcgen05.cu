@@ -194,46 +194,6 @@ struct BLayout {
   static constexpr int TILE = NHALF * HALF;
 };
 
-// The dK/dV kernel's element-wise step for one key row: from S^T (scores,
-// f32) and dP^T in tensor memory, P = exp2(S scale log2e - lse2) on the
-// valid columns and dS = P (dP - D); dS (and P when p_col >= 0) go back to
-// tensor memory as bf16 pairs.  lse2 / dlt give the per-column statistics
-// through the callables.  (Packed f32x2 arithmetic with paired statistics
-// loads measured 4 % slower here, so this step stays scalar.)
-template <typename LSE, typename DLT>
-__device__ __forceinline__ void p_ds_step(uint32_t t_s, uint32_t t_dp, int p_col, int ds_col,
-                                          const uint32_t (&w)[4], float sl2, LSE lse2, DLT dlt) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t x[32], y[32];
-    tmem_ld32(t_s + c * 32, x);
-    tmem_ld32(t_dp + c * 32, y);
-    tmem_wait_ld();
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      asm volatile("" : "+r"(x[k]));
-      asm volatile("" : "+r"(y[k]));
-    }
-    uint32_t pk[16], dk[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      float pv[2], dv[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int col = c * 32 + 2 * k + u;
-        const bool ok = (w[col >> 5] >> (col & 31)) & 1u;
-        const float e = ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), sl2, -lse2(col)));
-        pv[u] = ok ? e : 0.f;
-        dv[u] = pv[u] * (__uint_as_float(y[2 * k + u]) - dlt(col));
-      }
-      pk[k] = pack_bf16x2(pv[0], pv[1]);
-      dk[k] = pack_bf16x2(dv[0], dv[1]);
-    }
-    if (p_col >= 0) tmem_st16(t_s + p_col + c * 16, pk);
-    tmem_st16(t_s + ds_col + c * 16, dk);
-  }
-}
-
 template <int D>
 __device__ __forceinline__ void store_rows(void *base_ptr, bool f32, size_t off, const uint32_t (&r)[32],
                                            float mul) {
@@ -262,16 +222,32 @@ __device__ __forceinline__ void store_rows(void *base_ptr, bool f32, size_t off,
 // column, every query head of group g, both 128-row halves.  Tensor memory:
 // S^T [0,128)  dP^T [128,256)  dV [256,256+D)  dK [384,384+D); P^T and dS^T
 // (bf16) overwrite the first 64 columns of S^T and dP^T.
+//
+// The step is pipelined across two element-wise phases with their own
+// arrivals: phase P (P^T from S^T) and phase dS (dS^T from dP^T and P, kept
+// in registers).  The MMA lane issues, for step s,
+//   [P(s-1) arrived]  dV += P^T(s-1) dO(s-1),  S^T(s) = K Q(s)^T
+//   [dS(s-1) arrived] dK += dS^T(s-1) Q(s-1),  dP^T(s) = V dO(s)^T
+// so the tensor core computes dV and the next S^T while the element-wise
+// warps form dS, and dK and the next dP^T while they form the next P.  Each
+// new S^T (dP^T) overwrites columns the MMA issued just before it reads;
+// tcgen05 MMAs of one thread execute in issue order, and the element-wise
+// warps have read the old values before their arrival.  Q and dO stream
+// through two stages each, freed separately (dO after dV, Q after dK).
 template <int D>
 struct KVLayout {
   using B = BLayout<D>;
-  static constexpr int K_OFF = 0, V_OFF = B::TILE, ST_OFF = 2 * B::TILE;   // 2 stages of (Q, dO)
-  static constexpr int VEC_OFF = ST_OFF + 4 * B::TILE;                      // [2][lse2 128 | D 128]
+  static constexpr int K_OFF = 0, V_OFF = B::TILE;
+  static constexpr int Q_OFF = 2 * B::TILE, DO_OFF = 4 * B::TILE;            // 2 stages each
+  static constexpr int VEC_OFF = 6 * B::TILE;                                 // [2][lse2 128 | D 128]
   static constexpr int BAR_OFF = VEC_OFF + 2 * 256 * 4;
-  static constexpr int B_KV = 0, B_SF = 1, B_SE = 3, B_ST = 5, B_P = 6, B_O = 7, B_DR = 8, B_VEC = 9,
-                       NBAR = 10;
+  // kv | q_full[2] | q_empty[2] | do_full[2] | do_empty[2] | s_ready | dp_ready |
+  // p_done | ds_done | o_full | drain | vec
+  static constexpr int B_KV = 0, B_QF = 1, B_QE = 3, B_DF = 5, B_DE = 7, B_SR = 9, B_DPR = 10,
+                       B_PA = 11, B_DS = 12, B_O = 13, B_DR = 14, B_VEC = 15, NBAR = 16;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int ALLOC = MISC_OFF + 16 + 1024;
+  static_assert(ALLOC <= 232448, "shared memory per CTA");
 };
 
 template <int D>
@@ -301,11 +277,15 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_KV), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(L::B_SF + s), 1);
-      mbar_init(bar(L::B_SE + s), 1);
+      mbar_init(bar(L::B_QF + s), 1);
+      mbar_init(bar(L::B_QE + s), 1);
+      mbar_init(bar(L::B_DF + s), 1);
+      mbar_init(bar(L::B_DE + s), 1);
     }
-    mbar_init(bar(L::B_ST), 1);
-    mbar_init(bar(L::B_P), 128);
+    mbar_init(bar(L::B_SR), 1);
+    mbar_init(bar(L::B_DPR), 1);
+    mbar_init(bar(L::B_PA), 128);
+    mbar_init(bar(L::B_DS), 128);
     mbar_init(bar(L::B_O), 1);
     mbar_init(bar(L::B_DR), 1);
     mbar_init(bar(L::B_VEC), 128);
@@ -320,11 +300,26 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // the steps of this item: (column entry c, head offset hh, half t) with
-  // the half inside the query sequence
+  // the steps of this item: (column entry c, head offset gh, half t) with
+  // the half inside the query sequence, in this order
   auto half_ok = [&](int c, int t) { return p.col_q[c0 + c] * B_TILE_Q + t * 128 < p.sq; };
+  // moves (c, gh, t) to the next step; false past the last one
+  auto advance = [&](int &c, int &gh, int &t) -> bool {
+    do {
+      if (++t == 2) {
+        t = 0;
+        if (++gh == G) {
+          gh = 0;
+          ++c;
+        }
+      }
+      if (c >= nc) return false;
+    } while (!half_ok(c, t));
+    return true;
+  };
 
   if (warp == 4) {
+    // ------------------------------------------------------------ producer
     if (lane == 0 && nc > 0) {
       mbar_arrive_expect_tx(bar(L::B_KV), 2 * BL::TILE);
       for (int hh = 0; hh < BL::NHALF; ++hh) {
@@ -333,76 +328,125 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       }
       uint32_t s = 0;
       bool ok = true;
-      for (int c = 0; ok && c < nc; ++c)
-        for (int gh = 0; ok && gh < G; ++gh)
-          for (int t = 0; ok && t < 2; ++t) {
-            if (!half_ok(c, t)) continue;
-            const int st = s & 1;
-            if (s >= 2 && !mbar_wait_bounded(bar(L::B_SE + st), ((s >> 1) - 1) & 1, abort, lim)) {
-              ok = false;
-              break;
-            }
-            const int h = g * G + gh, q0 = p.col_q[c0 + c] * B_TILE_Q + t * 128;
-            const uint32_t dst = sb + L::ST_OFF + st * 2 * BL::TILE;
-            mbar_arrive_expect_tx(bar(L::B_SF + st), 2 * BL::TILE);
-            for (int hh = 0; hh < BL::NHALF; ++hh) {
-              tma_load_2d(dst + hh * BL::HALF, &tm_q, bar(L::B_SF + st), h * D + hh * 64, q0);
-              tma_load_2d(dst + BL::TILE + hh * BL::HALF, &tm_do, bar(L::B_SF + st), h * D + hh * 64, q0);
-            }
-            ++s;
-          }
+      int c = 0, gh = 0, t = -1;
+      while (ok && advance(c, gh, t)) {
+        const int st = s & 1;
+        const int h = g * G + gh, q0 = p.col_q[c0 + c] * B_TILE_Q + t * 128;
+        // Q(s) once dK(s-2) has read stage st, dO(s) once dV(s-2) has
+        if (s >= 2 && !mbar_wait_bounded(bar(L::B_QE + st), ((s >> 1) - 1) & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(L::B_QF + st), BL::TILE);
+        for (int hh = 0; hh < BL::NHALF; ++hh)
+          tma_load_2d(sb + L::Q_OFF + st * BL::TILE + hh * BL::HALF, &tm_q, bar(L::B_QF + st),
+                      h * D + hh * 64, q0);
+        if (s >= 2 && !mbar_wait_bounded(bar(L::B_DE + st), ((s >> 1) - 1) & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(L::B_DF + st), BL::TILE);
+        for (int hh = 0; hh < BL::NHALF; ++hh)
+          tma_load_2d(sb + L::DO_OFF + st * BL::TILE + hh * BL::HALF, &tm_do, bar(L::B_DF + st),
+                      h * D + hh * 64, q0);
+        ++s;
+      }
       if (*abort) {
+        // let the loads already in flight land before the CTA retires
         wait_drain(bar(L::B_KV), 0, 20000000ull);
-        for (uint32_t i = (s > 2 ? s - 2 : 0); i < s; ++i) wait_drain(bar(L::B_SF + (i & 1)), (i >> 1) & 1, 20000000ull);
+        for (uint32_t i = (s > 2 ? s - 2 : 0); i < s; ++i) {
+          wait_drain(bar(L::B_QF + (i & 1)), (i >> 1) & 1, 20000000ull);
+          wait_drain(bar(L::B_DF + (i & 1)), (i >> 1) & 1, 20000000ull);
+        }
       }
     }
   } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nc > 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 1);
       const uint32_t ks = sb + L::K_OFF, vs = sb + L::V_OFF;
+      auto qst = [&](uint32_t s) { return sb + L::Q_OFF + (s & 1) * BL::TILE; };
+      auto dost = [&](uint32_t s) { return sb + L::DO_OFF + (s & 1) * BL::TILE; };
+      // dV += P^T(s) dO(s), then dO's stage is free
+      auto issue_dv = [&](uint32_t s) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + 256, tmem + kk * 8, smem_desc_sw128(dost(s) + kk * 16 * 128, BL::HALF, 1024),
+                 IDESC_PV, (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::B_DE + (s & 1)));
+      };
+      // dK += dS^T(s) Q(s), then Q's stage is free
+      auto issue_dk = [&](uint32_t s) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + 384, tmem + 128 + kk * 8, smem_desc_sw128(qst(s) + kk * 16 * 128, BL::HALF, 1024),
+                 IDESC_PV, (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::B_QE + (s & 1)));
+      };
       bool ok = mbar_wait_bounded(bar(L::B_KV), 0, abort, lim);
       uint32_t s = 0;
-      for (int c = 0; ok && c < nc; ++c)
-        for (int gh = 0; ok && gh < G; ++gh)
-          for (int t = 0; ok && t < 2; ++t) {
-            if (!half_ok(c, t)) continue;
-            const int st = s & 1;
-            const uint32_t qs = sb + L::ST_OFF + st * 2 * BL::TILE, dos = qs + BL::TILE;
-            if (!mbar_wait_bounded(bar(L::B_SF + st), (s >> 1) & 1, abort, lim)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
-              mma_ss(tmem, smem_desc_sw128(ks + off, 16, 1024), smem_desc_sw128(qs + off, 16, 1024),
-                     IDESC_QK, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
-              mma_ss(tmem + 128, smem_desc_sw128(vs + off, 16, 1024),
-                     smem_desc_sw128(dos + off, 16, 1024), IDESC_QK, kk > 0);
-            }
-            mma_commit(bar(L::B_ST));
-            if (!mbar_wait_bounded(bar(L::B_P), s & 1, abort, lim)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              mma_ts(tmem + 256, tmem + kk * 8, smem_desc_sw128(dos + kk * 16 * 128, BL::HALF, 1024),
-                     IDESC_PV, (s > 0 || kk > 0) ? 1u : 0u);
-              mma_ts(tmem + 384, tmem + 128 + kk * 8, smem_desc_sw128(qs + kk * 16 * 128, BL::HALF, 1024),
-                     IDESC_PV, (s > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(bar(L::B_SE + st));
-            ++s;
+      int c = 0, gh = 0, t = -1;
+      while (ok && advance(c, gh, t)) {
+        if (s > 0) {
+          if (!mbar_wait_bounded(bar(L::B_PA), (s - 1) & 1, abort, lim)) {
+            ok = false;
+            break;
           }
-      if (ok) mma_commit(bar(L::B_O));
+          tc_fence_after();
+          issue_dv(s - 1);
+        }
+        if (!mbar_wait_bounded(bar(L::B_QF + (s & 1)), (s >> 1) & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // S^T(s) = K Q(s)^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
+          mma_ss(tmem, smem_desc_sw128(ks + off, 16, 1024), smem_desc_sw128(qst(s) + off, 16, 1024),
+                 IDESC_QK, kk > 0);
+        }
+        mma_commit(bar(L::B_SR));
+        if (s > 0) {
+          if (!mbar_wait_bounded(bar(L::B_DS), (s - 1) & 1, abort, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_dk(s - 1);
+        }
+        if (!mbar_wait_bounded(bar(L::B_DF + (s & 1)), (s >> 1) & 1, abort, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dP^T(s) = V dO(s)^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BL::HALF + (kk & 3) * 32;
+          mma_ss(tmem + 128, smem_desc_sw128(vs + off, 16, 1024), smem_desc_sw128(dost(s) + off, 16, 1024),
+                 IDESC_QK, kk > 0);
+        }
+        mma_commit(bar(L::B_DPR));
+        ++s;
+      }
+      if (ok && s > 0) {
+        // the last step's dV and dK
+        ok = mbar_wait_bounded(bar(L::B_PA), (s - 1) & 1, abort, lim);
+        if (ok) {
+          tc_fence_after();
+          issue_dv(s - 1);
+          ok = mbar_wait_bounded(bar(L::B_DS), (s - 1) & 1, abort, lim);
+        }
+        if (ok) {
+          tc_fence_after();
+          issue_dk(s - 1);
+          mma_commit(bar(L::B_O));
+        }
+      }
+      // every MMA this thread issued completes before tensor memory is freed
       mma_commit(bar(L::B_DR));
       wait_drain(bar(L::B_DR), 0, 20000000ull);
     }
@@ -412,53 +456,116 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     const int r = warp * 32 + lane;
     const int key = kt * 128 + r;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_dp = t_s + 128;
     const float sl2 = p.scale_log2;
     uint32_t s = 0;
     bool ok = true, any = false;
-    for (int c = 0; ok && c < nc; ++c) {
-      const int qt = p.col_q[c0 + c], e = p.col_e[c0 + c];
-      const int kd = p.kind[e], r0 = p.ref_ptr[e], r1 = p.ref_ptr[e + 1];
-      for (int gh = 0; ok && gh < G; ++gh)
-        for (int t = 0; ok && t < 2; ++t) {
-          if (!half_ok(c, t)) continue;
-          const int h = g * G + gh, q0 = qt * B_TILE_Q + t * 128;
-          float *vl = vec + (s & 1) * 256, *vd = vl + 128;
-          {
-            const int i = q0 + r;
-            const float lv = i < p.sq ? p.lse[static_cast<size_t>(h) * p.sq + i] : -INFINITY;
-            vl[r] = lv == -INFINITY ? INFINITY : lv * LOG2E;
-            vd[r] = i < p.sq ? p.delta[static_cast<size_t>(h) * p.sq + i] : 0.f;
-          }
-          // every element-wise thread has written its row's statistics
-          // (bounded wait: an abort elsewhere ends it)
-          mbar_arrive(bar(L::B_VEC));
-          if (!wait_all(bar(L::B_VEC), s & 1, abort, lim)) {
-            ok = false;
-            break;
-          }
-          uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-          if (kd == ATTN_TILE_MASKED) {
-            w[0] = w[1] = w[2] = w[3] = 0u;
-            for (int q = r0; q < r1; ++q) add_col_mask(p.slices[p.ref_idx[q]], key, q0, w);
-          }
-          if (!wait_all(bar(L::B_ST), s & 1, abort, lim)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          p_ds_step(tmem + lane_off, tmem + lane_off + 128, 0, 128, w, sl2,
-                    [&](int col) { return vl[col]; }, [&](int col) { return vd[col]; });
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(bar(L::B_P));
-          any = true;
-          ++s;
+    // this row's statistics of a step: log2-domain lse (+inf past S_q, so
+    // that P = 0 there) and D
+    auto load_stats = [&](int c, int gh, int t, float &lv, float &dv) {
+      const int h = g * G + gh, i = p.col_q[c0 + c] * B_TILE_Q + t * 128 + r;
+      const float l = i < p.sq ? p.lse[static_cast<size_t>(h) * p.sq + i] : -INFINITY;
+      lv = l == -INFINITY ? INFINITY : l * LOG2E;
+      dv = i < p.sq ? p.delta[static_cast<size_t>(h) * p.sq + i] : 0.f;
+    };
+    int c = 0, gh = 0, t = -1;
+    bool have = advance(c, gh, t);
+    float lv = 0.f, dv = 0.f;
+    if (have) load_stats(c, gh, t, lv, dv);
+    while (ok && have) {
+      const int q0 = p.col_q[c0 + c] * B_TILE_Q + t * 128, e = p.col_e[c0 + c];
+      const float *vl = vec + (s & 1) * 256, *vd = vl + 128;
+      // every element-wise thread has written its row's statistics of this
+      // step (the buffer of step s - 2 is free: all threads got past step
+      // s - 1's barrier, after their last reads of it)
+      vec[(s & 1) * 256 + r] = lv;
+      vec[(s & 1) * 256 + 128 + r] = dv;
+      mbar_arrive(bar(L::B_VEC));
+      if (!wait_all(bar(L::B_VEC), s & 1, abort, lim)) {
+        ok = false;
+        break;
+      }
+      uint32_t w[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      if (p.kind[e] == ATTN_TILE_MASKED) {
+        w[0] = w[1] = w[2] = w[3] = 0u;
+        const int r0 = p.ref_ptr[e], r1 = p.ref_ptr[e + 1];
+        for (int q = r0; q < r1; ++q) add_col_mask(p.slices[p.ref_idx[q]], key, q0, w);
+      }
+      // ---- phase P: P = exp2(S scale log2e - lse2) on the valid columns,
+      // kept in f32 for phase dS; P^T (bf16) over S^T's first 64 columns
+      if (!wait_all(bar(L::B_SR), s & 1, abort, lim)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float P[128];
+      {
+        uint32_t x[128];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[cc * 32]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 128; ++k) {
+          asm volatile("" : "+r"(x[k]));
+          P[k] = __uint_as_float(x[k]);
         }
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int col = cc * 32 + k;
+          const bool okc = (w[cc] >> k) & 1u;
+          const float ev = ex2_approx(fmaf(P[col], sl2, -vl[col]));
+          P[col] = okc ? ev : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(P[cc * 32 + 2 * k], P[cc * 32 + 2 * k + 1]);
+        tmem_st16(t_s + cc * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(L::B_PA));
+      // the next step's statistics load while phase dS runs
+      int c2 = c, gh2 = gh, t2 = t;
+      const bool have2 = advance(c2, gh2, t2);
+      if (have2) load_stats(c2, gh2, t2, lv, dv);
+      // ---- phase dS: dS = P (dP - D); dS^T (bf16) over dP^T's first 64
+      // columns (chunk cc writes columns chunk cc - 1 and cc have been read from)
+      if (!wait_all(bar(L::B_DPR), s & 1, abort, lim)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t y[32];
+        tmem_ld32_wait(t_dp + cc * 32, y);
+        uint32_t dk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int col = cc * 32 + 2 * k;
+          const float d0 = P[col] * (__uint_as_float(y[2 * k]) - vd[col]);
+          const float d1 = P[col + 1] * (__uint_as_float(y[2 * k + 1]) - vd[col + 1]);
+          dk[k] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(t_dp + cc * 16, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(L::B_DS));
+      any = true;
+      ++s;
+      c = c2;
+      gh = gh2;
+      t = t2;
+      have = have2;
     }
     // ---------------------------------------------------------- epilogue
-    bool have = ok && any;
-    if (have) {
-      have = wait_all(bar(L::B_O), 0, abort, lim);
+    bool have_o = ok && any;
+    if (have_o) {
+      have_o = wait_all(bar(L::B_O), 0, abort, lim);
       tc_fence_after();
     }
     if (ok) {
@@ -467,7 +574,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t rv[32], rk[32];
-        if (have) {
+        if (have_o) {
           tmem_ld32_wait(tmem + lane_off + 256 + cc * 32, rv);
           tmem_ld32_wait(tmem + lane_off + 384 + cc * 32, rk);
         } else {
