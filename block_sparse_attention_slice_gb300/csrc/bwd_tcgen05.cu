@@ -33,7 +33,8 @@ namespace attn {
 // ATTN_OK.  Read and cleared by attn_last_device_error().
 __device__ unsigned int g_bwd_status;
 
-constexpr int B_THREADS = 192;     // warps 0-3 element-wise, 4 producer, 5 MMA issuer
+constexpr int B_THREADS = 192;     // dQ kernel: warps 0-3 element-wise, 4 producer, 5 MMA issuer
+constexpr int KV_THREADS = 320;    // dK/dV kernel: warps 0-7 element-wise, 8 producer, 9 MMA issuer
 constexpr int B_TILE_Q = 256;      // query rows per tile of the metadata
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -251,7 +252,7 @@ struct KVLayout {
 };
 
 template <int D>
-__global__ void __launch_bounds__(B_THREADS, 1)
+__global__ void __launch_bounds__(KV_THREADS, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
@@ -284,15 +285,15 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     }
     mbar_init(bar(L::B_SR), 1);
     mbar_init(bar(L::B_DPR), 1);
-    mbar_init(bar(L::B_PA), 128);
-    mbar_init(bar(L::B_DS), 128);
+    mbar_init(bar(L::B_PA), 256);
+    mbar_init(bar(L::B_DS), 256);
     mbar_init(bar(L::B_O), 1);
     mbar_init(bar(L::B_DR), 1);
-    mbar_init(bar(L::B_VEC), 128);
+    mbar_init(bar(L::B_VEC), 256);
     *abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     return true;
   };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && nc > 0) {
       mbar_arrive_expect_tx(bar(L::B_KV), 2 * BL::TILE);
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nc > 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0);
@@ -372,7 +373,8 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       auto issue_dv = [&](uint32_t s) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + 256, tmem + kk * 8, smem_desc_sw128(dost(s) + kk * 16 * 128, BL::HALF, 1024),
+          mma_ts(tmem + 256, tmem + (kk >> 2) * 64 + (kk & 3) * 8,
+                 smem_desc_sw128(dost(s) + kk * 16 * 128, BL::HALF, 1024),
                  IDESC_PV, (s > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::B_DE + (s & 1)));
       };
@@ -380,7 +382,8 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       auto issue_dk = [&](uint32_t s) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + 384, tmem + 128 + kk * 8, smem_desc_sw128(qst(s) + kk * 16 * 128, BL::HALF, 1024),
+          mma_ts(tmem + 384, tmem + 128 + (kk >> 2) * 64 + (kk & 3) * 8,
+                 smem_desc_sw128(qst(s) + kk * 16 * 128, BL::HALF, 1024),
                  IDESC_PV, (s > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::B_QE + (s & 1)));
       };
@@ -453,15 +456,17 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ element-wise (thread = key row)
-    const int r = warp * 32 + lane;
+    // warps 0-3 and 4-7 take the same 128 key rows (tensor-memory lanes
+    // 32 (warp % 4) ...), columns (queries) [64 hc, 64 hc + 64) each
+    const int r = (warp & 3) * 32 + lane, hc = warp >> 2;
     const int key = kt * 128 + r;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_off, t_dp = t_s + 128;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + hc * 64, t_dp = t_s + 128;
     const float sl2 = p.scale_log2;
     uint32_t s = 0;
     bool ok = true, any = false;
-    // this row's statistics of a step: log2-domain lse (+inf past S_q, so
-    // that P = 0 there) and D
+    // statistics of query row q0 + r of a step (warps 0-3 stage all 128):
+    // log2-domain lse (+inf past S_q, so that P = 0 there) and D
     auto load_stats = [&](int c, int gh, int t, float &lv, float &dv) {
       const int h = g * G + gh, i = p.col_q[c0 + c] * B_TILE_Q + t * 128 + r;
       const float l = i < p.sq ? p.lse[static_cast<size_t>(h) * p.sq + i] : -INFINITY;
@@ -471,15 +476,17 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     int c = 0, gh = 0, t = -1;
     bool have = advance(c, gh, t);
     float lv = 0.f, dv = 0.f;
-    if (have) load_stats(c, gh, t, lv, dv);
+    if (have && hc == 0) load_stats(c, gh, t, lv, dv);
     while (ok && have) {
       const int q0 = p.col_q[c0 + c] * B_TILE_Q + t * 128, e = p.col_e[c0 + c];
-      const float *vl = vec + (s & 1) * 256, *vd = vl + 128;
-      // every element-wise thread has written its row's statistics of this
-      // step (the buffer of step s - 2 is free: all threads got past step
-      // s - 1's barrier, after their last reads of it)
-      vec[(s & 1) * 256 + r] = lv;
-      vec[(s & 1) * 256 + 128 + r] = dv;
+      const float *vl = vec + (s & 1) * 256 + hc * 64, *vd = vl + 128;
+      // the statistics of this step are staged (the buffer of step s - 2 is
+      // free: every element-wise thread got past step s - 1's barrier, after
+      // its last reads of it)
+      if (hc == 0) {
+        vec[(s & 1) * 256 + r] = lv;
+        vec[(s & 1) * 256 + 128 + r] = dv;
+      }
       mbar_arrive(bar(L::B_VEC));
       if (!wait_all(bar(L::B_VEC), s & 1, abort, lim)) {
         ok = false;
@@ -491,38 +498,39 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         const int r0 = p.ref_ptr[e], r1 = p.ref_ptr[e + 1];
         for (int q = r0; q < r1; ++q) add_col_mask(p.slices[p.ref_idx[q]], key, q0, w);
       }
+      const uint32_t wm[2] = {hc ? w[2] : w[0], hc ? w[3] : w[1]};
       // ---- phase P: P = exp2(S scale log2e - lse2) on the valid columns,
-      // kept in f32 for phase dS; P^T (bf16) over S^T's first 64 columns
+      // kept in f32 for phase dS; P^T (bf16) over the first 32 of this
+      // warp's 64 S^T columns
       if (!wait_all(bar(L::B_SR), s & 1, abort, lim)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float P[128];
+      float P[64];
       {
-        uint32_t x[128];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[cc * 32]));
+        uint32_t x[64];
+        tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 128; ++k) {
+        for (int k = 0; k < 64; ++k) {
           asm volatile("" : "+r"(x[k]));
           P[k] = __uint_as_float(x[k]);
         }
       }
+      {
+        uint32_t pk[32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int col = cc * 32 + k;
-          const bool okc = (w[cc] >> k) & 1u;
-          const float ev = ex2_approx(fmaf(P[col], sl2, -vl[col]));
-          P[col] = okc ? ev : 0.f;
+        for (int k = 0; k < 64; ++k) {
+          const bool okc = (wm[k >> 5] >> (k & 31)) & 1u;
+          const float ev = ex2_approx(fmaf(P[k], sl2, -vl[k]));
+          P[k] = okc ? ev : 0.f;
         }
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(P[cc * 32 + 2 * k], P[cc * 32 + 2 * k + 1]);
-        tmem_st16(t_s + cc * 16, pk);
+        for (int k = 0; k < 32; ++k) pk[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
+        tmem_st16(t_s, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(t_s + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
       }
       tmem_wait_st();
       tc_fence_before();
@@ -530,27 +538,30 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       // the next step's statistics load while phase dS runs
       int c2 = c, gh2 = gh, t2 = t;
       const bool have2 = advance(c2, gh2, t2);
-      if (have2) load_stats(c2, gh2, t2, lv, dv);
-      // ---- phase dS: dS = P (dP - D); dS^T (bf16) over dP^T's first 64
-      // columns (chunk cc writes columns chunk cc - 1 and cc have been read from)
+      if (have2 && hc == 0) load_stats(c2, gh2, t2, lv, dv);
+      // ---- phase dS: dS = P (dP - D); dS^T (bf16) over the first 32 of this
+      // warp's 64 dP^T columns
       if (!wait_all(bar(L::B_DPR), s & 1, abort, lim)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      {
+        uint32_t y[64];
+        tmem_ld32(t_dp, *reinterpret_cast<uint32_t(*)[32]>(&y[0]));
+        tmem_ld32(t_dp + 32, *reinterpret_cast<uint32_t(*)[32]>(&y[32]));
+        tmem_wait_ld();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t y[32];
-        tmem_ld32_wait(t_dp + cc * 32, y);
-        uint32_t dk[16];
+        for (int k = 0; k < 64; ++k) asm volatile("" : "+r"(y[k]));
+        uint32_t dk[32];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int col = cc * 32 + 2 * k;
-          const float d0 = P[col] * (__uint_as_float(y[2 * k]) - vd[col]);
-          const float d1 = P[col + 1] * (__uint_as_float(y[2 * k + 1]) - vd[col + 1]);
+        for (int k = 0; k < 32; ++k) {
+          const float d0 = P[2 * k] * (__uint_as_float(y[2 * k]) - vd[2 * k]);
+          const float d1 = P[2 * k + 1] * (__uint_as_float(y[2 * k + 1]) - vd[2 * k + 1]);
           dk[k] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(t_dp + cc * 16, dk);
+        tmem_st16(t_dp, *reinterpret_cast<const uint32_t(*)[16]>(&dk[0]));
+        tmem_st16(t_dp + 16, *reinterpret_cast<const uint32_t(*)[16]>(&dk[16]));
       }
       tmem_wait_st();
       tc_fence_before();
@@ -563,6 +574,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       have = have2;
     }
     // ---------------------------------------------------------- epilogue
+    // columns [hc D / 2, hc D / 2 + D / 2) of this row's dV and dK
     bool have_o = ok && any;
     if (have_o) {
       have_o = wait_all(bar(L::B_O), 0, abort, lim);
@@ -571,12 +583,13 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     if (ok) {
       // tensor-memory loads stay warp-uniform; only the stores depend on the row
       const size_t off = (static_cast<size_t>(key) * p.hk + g) * D;
+      const uint32_t row_t = tmem + lane_off;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = hc * (D / 64); cc < (hc + 1) * (D / 64); ++cc) {
         uint32_t rv[32], rk[32];
         if (have_o) {
-          tmem_ld32_wait(tmem + lane_off + 256 + cc * 32, rv);
-          tmem_ld32_wait(tmem + lane_off + 384 + cc * 32, rk);
+          tmem_ld32_wait(row_t + 256 + cc * 32, rv);
+          tmem_ld32_wait(row_t + 384 + cc * 32, rk);
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) rv[k] = rk[k] = 0u;
@@ -592,7 +605,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == 9) tmem_dealloc(tmem, 512);
   if (threadIdx.x == 0 && *abort) atomicCAS(&g_bwd_status, 0u, static_cast<unsigned>(ATTN_ERR_TIMEOUT));
 }
 
@@ -916,7 +929,7 @@ static int launch_bwd_main(const CUtensorMap *m, const BwdParams &p, cudaStream_
   if ((rc = set_smem(bwd_kv_kernel<D>, KVLayout<D>::ALLOC)) != ATTN_OK) return rc;
   if ((rc = set_smem(bwd_q_kernel<D, NS>, QLayout<D, NS>::ALLOC)) != ATTN_OK) return rc;
   if (p.n_ktiles > 0)
-    bwd_kv_kernel<D><<<p.n_ktiles * p.hk, B_THREADS, KVLayout<D>::ALLOC, s>>>(m[0], m[1], m[2], m[3], p);
+    bwd_kv_kernel<D><<<p.n_ktiles * p.hk, KV_THREADS, KVLayout<D>::ALLOC, s>>>(m[0], m[1], m[2], m[3], p);
   if (p.n_qtiles > 0)
     bwd_q_kernel<D, NS><<<p.n_qtiles * p.hq, B_THREADS, QLayout<D, NS>::ALLOC, s>>>(m[0], m[1], m[2], m[3], p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
