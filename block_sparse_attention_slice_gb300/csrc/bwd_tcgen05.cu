@@ -33,7 +33,7 @@ namespace attn {
 // ATTN_OK.  Read and cleared by attn_last_device_error().
 __device__ unsigned int g_bwd_status;
 
-constexpr int B_THREADS = 192;     // dQ kernel: warps 0-3 element-wise, 4 producer, 5 MMA issuer
+constexpr int Q_THREADS = 192;     // dQ kernel: warps 0-3 element-wise, 4 producer, 5 MMA issuer
 constexpr int KV_THREADS = 320;    // dK/dV kernel: warps 0-7 element-wise, 8 producer, 9 MMA issuer
 constexpr int B_TILE_Q = 256;      // query rows per tile of the metadata
 constexpr float LOG2E = 1.4426950408889634f;
@@ -678,7 +678,7 @@ __device__ __forceinline__ void ds_step_dp_first(uint32_t t_s, uint32_t t_dp, bo
 }
 
 template <int D, int NS>
-__global__ void __launch_bounds__(B_THREADS, 1)
+__global__ void __launch_bounds__(Q_THREADS, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                  const BwdParams p) {
@@ -931,7 +931,7 @@ static int launch_bwd_main(const CUtensorMap *m, const BwdParams &p, cudaStream_
   if (p.n_ktiles > 0)
     bwd_kv_kernel<D><<<p.n_ktiles * p.hk, KV_THREADS, KVLayout<D>::ALLOC, s>>>(m[0], m[1], m[2], m[3], p);
   if (p.n_qtiles > 0)
-    bwd_q_kernel<D, NS><<<p.n_qtiles * p.hq, B_THREADS, QLayout<D, NS>::ALLOC, s>>>(m[0], m[1], m[2], m[3], p);
+    bwd_q_kernel<D, NS><<<p.n_qtiles * p.hq, Q_THREADS, QLayout<D, NS>::ALLOC, s>>>(m[0], m[1], m[2], m[3], p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
