@@ -471,7 +471,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           else mma_ts(d_tmem, a_tmem + kk * 8, b, IDESC_PV, (first && kk == 0) ? 0u : 1u);
         }
       };
-      uint32_t ld = 0, nonempty = 0, step = 0;
+      uint32_t rs = 0, rp = 0, nonempty = 0, step = 0;
+      auto ring_next = [](uint32_t &slot, uint32_t &phase) {
+        if (++slot == static_cast<uint32_t>(NS)) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      };
       bool ok = true;
       uint32_t qpos = 0;
       while (ok) {
@@ -485,38 +491,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         arrive0(L::B_IE + qs);
         ++qpos;
         if (item >= p.n_items) break;
-        const Item it = from_slot(p, qi, *order != 0);
-        const int n = it.n;
+        // only the entry count matters here (no head decode on this path)
+        const int n = qi.n;
         if (n == 0) continue;
-        ok = waitb(bar(L::B_Q), nonempty & 1) &&
-             waitb(bar(L::B_FULL + ld % NS), (ld / NS) & 1);
+        // ring position ld as (slot, phase), advanced incrementally: no
+        // division by NS on the issuing thread's path between MMA groups
+        const uint32_t s0 = rs, p0 = rp;
+        ok = waitb(bar(L::B_Q), nonempty & 1) && waitb(bar(L::B_FULL + s0), p0);
         if (!ok) break;
         tc_fence_after();
-        issue_qk(0, ld % NS);
+        issue_qk(0, s0);
         commit(bar(L::B_S + 0));
-        issue_qk(1, ld % NS);
+        issue_qk(1, s0);
         commit(bar(L::B_S + 1));
-        commit(bar(L::B_EMPTY + ld % NS));
+        commit(bar(L::B_EMPTY + s0));
         if (n == 1) commit(bar(L::B_QE));
-        ++ld;
+        ring_next(rs, rp);
         for (int j = 0; j < n; ++j, ++step) {
-          const uint32_t vpos = ld, kpos = ld + 1;
+          const uint32_t vs = rs, vp = rp;
+          uint32_t ks = rs, kp = rp;
+          ring_next(ks, kp);
           const bool more = j + 1 < n;
-          if (!waitb(bar(L::B_FULL + vpos % NS), (vpos / NS) & 1) ||
+          if (!waitb(bar(L::B_FULL + vs), vp) ||
               !waitc(bar(L::B_P + 0), step & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(0, vpos % NS, j == 0);
+          issue_pv(0, vs, j == 0);
           if (!more) commit(bar(L::B_O + 0));
           if (more) {
-            if (!waitb(bar(L::B_FULL + kpos % NS), (kpos / NS) & 1)) {
+            if (!waitb(bar(L::B_FULL + ks), kp)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_qk(0, kpos % NS);
+            issue_qk(0, ks);
             commit(bar(L::B_S + 0));
           }
           if (!waitc(bar(L::B_P + 1), step & 1)) {
@@ -524,16 +534,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             break;
           }
           tc_fence_after();
-          issue_pv(1, vpos % NS, j == 0);
-          commit(bar(L::B_EMPTY + vpos % NS));
+          issue_pv(1, vs, j == 0);
+          commit(bar(L::B_EMPTY + vs));
           if (!more) commit(bar(L::B_O + 1));
           if (more) {
-            issue_qk(1, kpos % NS);
+            issue_qk(1, ks);
             commit(bar(L::B_S + 1));
-            commit(bar(L::B_EMPTY + kpos % NS));
+            commit(bar(L::B_EMPTY + ks));
             if (j + 2 == n) commit(bar(L::B_QE));
           }
-          ld += more ? 2 : 1;
+          rs = more ? ks : rs;
+          rp = more ? kp : rp;
+          ring_next(rs, rp);
         }
         ++nonempty;
       }
