@@ -303,7 +303,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   // the steps of this item: (column entry c, head offset gh, half t) with
   // the half inside the query sequence, in this order
-  auto half_ok = [&](int c, int t) { return p.col_q[c0 + c] * B_TILE_Q + t * 128 < p.sq; };
+  // (the first half of a query tile always lies inside S_q: only the second
+  // one needs the tile's index)
+  auto half_ok = [&](int c, int t) { return t == 0 || p.col_q[c0 + c] * B_TILE_Q + 128 < p.sq; };
   // moves (c, gh, t) to the next step; false past the last one
   auto advance = [&](int &c, int &gh, int &t) -> bool {
     do {
@@ -765,10 +767,6 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 1);
       const uint32_t qs = sb + L::Q_OFF, dos = sb + L::DO_OFF;
-      auto slot = [=](uint32_t pos) -> uint32_t { return sb + L::KV_OFF + (pos % NS) * BL::TILE; };
-      auto full = [=](uint32_t pos) -> bool {
-        return mbar_wait_bounded(bar(L::B_FULL + pos % NS), (pos / NS) & 1, abort, lim);
-      };
       // S(j) = Q K^T and dP = dO V^T (SS); dQ += dS(j) K (TS, K MN-major)
       auto mma_s = [=](int j, uint32_t kb) {
 #pragma unroll
@@ -792,39 +790,66 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
           mma_ts(tmem + 256, tmem + q_s_col(j) + kk * 8, smem_desc_sw128(kb + kk * 16 * 128, BL::HALF, 1024),
                  IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
       };
-      // ring positions of a half: K_j at ld + 2j, V_j at ld + 2j + 1
-      uint32_t ld = 0, s = 0;
+      // ring positions of a half: K_j at ld + 2j, V_j at ld + 2j + 1.  The
+      // position ld + 2j is kept as (slot bs, round br), advanced by 2 per
+      // key tile, and ld + 2j + off (off <= 4 < NS) as one conditional
+      // subtraction: no division by NS on the issuing thread's path.
+      uint32_t bs = 0, br = 0, s = 0;
+      auto at = [&](uint32_t off, uint32_t &sl, uint32_t &ph) {
+        sl = bs + off;
+        uint32_t r = br;
+        if (sl >= static_cast<uint32_t>(NS)) {
+          sl -= NS;
+          ++r;
+        }
+        ph = r & 1u;
+      };
+      auto full_at = [&](uint32_t off, uint32_t &sl) -> bool {
+        uint32_t ph;
+        at(off, sl, ph);
+        return mbar_wait_bounded(bar(L::B_FULL + sl), ph, abort, lim);
+      };
+      auto kv_at = [=](uint32_t sl) -> uint32_t { return sb + L::KV_OFF + sl * BL::TILE; };
+      auto step2 = [&]() {
+        bs += 2;
+        if (bs >= static_cast<uint32_t>(NS)) {
+          bs -= NS;
+          ++br;
+        }
+      };
       bool ok = true;
       for (int t = 0; ok && t < halves; ++t) {
-        ok = mbar_wait_bounded(bar(L::B_Q), t & 1, abort, lim) && full(ld) && full(ld + 1);
+        uint32_t s0, s1;
+        ok = mbar_wait_bounded(bar(L::B_Q), t & 1, abort, lim) && full_at(0, s0) && full_at(1, s1);
         if (!ok) break;
         tc_fence_after();
-        mma_s(0, slot(ld));
-        mma_dp(slot(ld + 1));
+        mma_s(0, kv_at(s0));
+        mma_dp(kv_at(s1));
         mma_commit(bar(L::B_S));
-        mma_commit(bar(L::B_EMPTY + (ld + 1) % NS));
+        mma_commit(bar(L::B_EMPTY + s1));
         if (n == 1) mma_commit(bar(L::B_QE));
         if (n > 1) {
-          if (!full(ld + 2)) {
+          uint32_t s2;
+          if (!full_at(2, s2)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          mma_s(1, slot(ld + 2));
+          mma_s(1, kv_at(s2));
         }
-        for (int j = 0; j < n; ++j, ++s) {
-          const uint32_t kj = ld + 2u * j;
+        for (int j = 0; j < n; ++j, ++s, step2()) {
           if (j + 1 < n) {
             // dP(j+1) once dP(j) is in the element-wise warps' registers;
             // this commit also covers S(j+1), issued one key tile earlier
-            if (!full(kj + 3) || !mbar_wait_bounded(bar(L::B_DPR), s & 1, abort, lim)) {
+            uint32_t s3;
+            if (!full_at(3, s3) || !mbar_wait_bounded(bar(L::B_DPR), s & 1, abort, lim)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            mma_dp(slot(kj + 3));
+            mma_dp(kv_at(s3));
             mma_commit(bar(L::B_S));
-            mma_commit(bar(L::B_EMPTY + (kj + 3) % NS));
+            mma_commit(bar(L::B_EMPTY + s3));
             if (j + 2 == n) mma_commit(bar(L::B_QE));   // the half's last reads of Q and dO
           }
           if (!mbar_wait_bounded(bar(L::B_P), s & 1, abort, lim)) {
@@ -832,19 +857,19 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             break;
           }
           tc_fence_after();
-          mma_dq(j, slot(kj));
-          mma_commit(bar(L::B_EMPTY + kj % NS));
+          mma_dq(j, kv_at(bs));
+          mma_commit(bar(L::B_EMPTY + bs));
           if (j + 2 < n) {
-            if (!full(kj + 4)) {
+            uint32_t s4;
+            if (!full_at(4, s4)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            mma_s(j + 2, slot(kj + 4));
+            mma_s(j + 2, kv_at(s4));
           }
         }
         if (ok) mma_commit(bar(L::B_O));
-        ld += 2u * n;
       }
       mma_commit(bar(L::B_DR));
       wait_drain(bar(L::B_DR), 0, 20000000ull);

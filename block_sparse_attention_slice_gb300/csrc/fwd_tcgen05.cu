@@ -512,8 +512,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           uint32_t ks = rs, kp = rp;
           ring_next(ks, kp);
           const bool more = j + 1 < n;
-          if (!waitb(bar(L::B_FULL + vs), vp) ||
-              !waitc(bar(L::B_P + 0), step & 1)) {
+          // both phases tested at once (their latencies overlap); the
+          // bounded waits only where one is not complete yet
+          const bool have_v = mbar_try_wait(bar(L::B_FULL + vs), vp);
+          const bool have_p = !PAIR && mbar_try_wait(bar(L::B_P + 0), step & 1);
+          if ((!have_v && !waitb(bar(L::B_FULL + vs), vp)) ||
+              (!have_p && !waitc(bar(L::B_P + 0), step & 1))) {
             ok = false;
             break;
           }
