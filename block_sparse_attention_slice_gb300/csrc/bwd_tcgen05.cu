@@ -393,15 +393,21 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       uint32_t s = 0;
       int c = 0, gh = 0, t = -1;
       while (ok && advance(c, gh, t)) {
+        // each group's dependency is tested (blocking) together with a
+        // non-blocking look at the next group's: their latencies overlap,
+        // and the next wait is skipped when the look found it complete
+        bool have_q = false, have_do = false;
         if (s > 0) {
-          if (!mbar_wait_bounded(bar(L::B_PA), (s - 1) & 1, abort, lim)) {
+          const bool have_p = mbar_try_wait(bar(L::B_PA), (s - 1) & 1);
+          have_q = mbar_test_wait(bar(L::B_QF + (s & 1)), (s >> 1) & 1);
+          if (!have_p && !mbar_wait_bounded(bar(L::B_PA), (s - 1) & 1, abort, lim)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_dv(s - 1);
         }
-        if (!mbar_wait_bounded(bar(L::B_QF + (s & 1)), (s >> 1) & 1, abort, lim)) {
+        if (!have_q && !mbar_wait_bounded(bar(L::B_QF + (s & 1)), (s >> 1) & 1, abort, lim)) {
           ok = false;
           break;
         }
@@ -415,14 +421,16 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         }
         mma_commit(bar(L::B_SR));
         if (s > 0) {
-          if (!mbar_wait_bounded(bar(L::B_DS), (s - 1) & 1, abort, lim)) {
+          const bool have_ds = mbar_try_wait(bar(L::B_DS), (s - 1) & 1);
+          have_do = mbar_test_wait(bar(L::B_DF + (s & 1)), (s >> 1) & 1);
+          if (!have_ds && !mbar_wait_bounded(bar(L::B_DS), (s - 1) & 1, abort, lim)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_dk(s - 1);
         }
-        if (!mbar_wait_bounded(bar(L::B_DF + (s & 1)), (s >> 1) & 1, abort, lim)) {
+        if (!have_do && !mbar_wait_bounded(bar(L::B_DF + (s & 1)), (s >> 1) & 1, abort, lim)) {
           ok = false;
           break;
         }
@@ -838,11 +846,19 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
           mma_s(1, kv_at(s2));
         }
         for (int j = 0; j < n; ++j, ++s, step2()) {
+          bool have_p = false;
           if (j + 1 < n) {
             // dP(j+1) once dP(j) is in the element-wise warps' registers;
-            // this commit also covers S(j+1), issued one key tile earlier
-            uint32_t s3;
-            if (!full_at(3, s3) || !mbar_wait_bounded(bar(L::B_DPR), s & 1, abort, lim)) {
+            // this commit also covers S(j+1), issued one key tile earlier.
+            // Both dependencies are tested together (blocking), with a
+            // non-blocking look at P(j) for the group after.
+            uint32_t s3, ph3;
+            at(3, s3, ph3);
+            const bool have_v = mbar_try_wait(bar(L::B_FULL + s3), ph3);
+            const bool have_dpr = mbar_try_wait(bar(L::B_DPR), s & 1);
+            have_p = mbar_test_wait(bar(L::B_P), s & 1);
+            if ((!have_v && !mbar_wait_bounded(bar(L::B_FULL + s3), ph3, abort, lim)) ||
+                (!have_dpr && !mbar_wait_bounded(bar(L::B_DPR), s & 1, abort, lim))) {
               ok = false;
               break;
             }
@@ -852,7 +868,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             mma_commit(bar(L::B_EMPTY + s3));
             if (j + 2 == n) mma_commit(bar(L::B_QE));   // the half's last reads of Q and dO
           }
-          if (!mbar_wait_bounded(bar(L::B_P), s & 1, abort, lim)) {
+          if (!have_p && !mbar_wait_bounded(bar(L::B_P), s & 1, abort, lim)) {
             ok = false;
             break;
           }

@@ -497,7 +497,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ring position ld as (slot, phase), advanced incrementally: no
         // division by NS on the issuing thread's path between MMA groups
         const uint32_t s0 = rs, p0 = rp;
-        ok = waitb(bar(L::B_Q), nonempty & 1) && waitb(bar(L::B_FULL + s0), p0);
+        {
+          const bool have_q = mbar_try_wait(bar(L::B_Q), nonempty & 1);
+          const bool have_k0 = mbar_try_wait(bar(L::B_FULL + s0), p0);
+          ok = (have_q || waitb(bar(L::B_Q), nonempty & 1)) && (have_k0 || waitb(bar(L::B_FULL + s0), p0));
+        }
         if (!ok) break;
         tc_fence_after();
         issue_qk(0, s0);
@@ -523,9 +527,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           tc_fence_after();
           issue_pv(0, vs, j == 0);
+          bool have_p1 = false;
           if (!more) commit(bar(L::B_O + 0));
           if (more) {
-            if (!waitb(bar(L::B_FULL + ks), kp)) {
+            // K_{j+1} (blocking) and P_1(j) (a non-blocking look) tested back
+            // to back, ahead of QK_0(j+1)
+            const bool have_k = mbar_try_wait(bar(L::B_FULL + ks), kp);
+            have_p1 = !PAIR && mbar_test_wait(bar(L::B_P + 1), step & 1);
+            if (!have_k && !waitb(bar(L::B_FULL + ks), kp)) {
               ok = false;
               break;
             }
@@ -533,7 +542,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             issue_qk(0, ks);
             commit(bar(L::B_S + 0));
           }
-          if (!waitc(bar(L::B_P + 1), step & 1)) {
+          if (!have_p1 && !waitc(bar(L::B_P + 1), step & 1)) {
             ok = false;
             break;
           }
