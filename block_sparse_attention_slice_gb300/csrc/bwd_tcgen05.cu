@@ -390,9 +390,14 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         mma_commit(bar(L::B_QE + (s & 1)));
       };
       bool ok = mbar_wait_bounded(bar(L::B_KV), 0, abort, lim);
+      // The issuer needs only the number of steps: every column entry has
+      // both halves for each of the G heads, except that the last query tile
+      // (the column's last entry, if it has it) may lack its second half.
+      const int last_q = (p.sq - 1) / B_TILE_Q;
+      const bool short_last = p.col_q[c0 + nc - 1] == last_q && !half_ok(nc - 1, 1);
+      const uint32_t nsteps = static_cast<uint32_t>(nc * 2 * G - (short_last ? G : 0));
       uint32_t s = 0;
-      int c = 0, gh = 0, t = -1;
-      while (ok && advance(c, gh, t)) {
+      for (; ok && s < nsteps;) {
         // each group's dependency is tested (blocking) together with a
         // non-blocking look at the next group's: their latencies overlap,
         // and the next wait is skipped when the look found it complete
