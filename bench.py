@@ -495,6 +495,13 @@ def gpu_arm(args, ws, rank, local):
         rc = pkg.attn_last_device_error()
         if rc != 0:
             raise RuntimeError(f"device status {rc} in the end-to-end region")
+        # the last step's result, read back to the host, must equal the
+        # device-timed step's (same inputs and kernels): a check of the
+        # streams' and events' ordering (outside the timed region)
+        last = slots[(n_e2e - 1) % nslot]
+        ref_o, ref_l = (mout, mlse) if split else (out, lse)
+        if not (torch.equal(last["oh"], ref_o.cpu()) and torch.equal(last["lh"], ref_l.cpu())):
+            raise RuntimeError("end-to-end result differs from the device-timed step's")
         e2e_ms = reduce_max(es.elapsed_time(ee) / n_e2e, ws, dev)
         h2d = (q.numel() + k.numel() + v.numel()) * 2 + sum(int(x[1]) * 20 for x in [prep] + [s[1] for s in split])
         d2h = out.numel() * 2 + lse.numel() * 4
