@@ -851,7 +851,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
           mma_s(1, kv_at(s2));
         }
         for (int j = 0; j < n; ++j, ++s, step2()) {
-          bool have_p = false;
+          bool have_p = false, look_k = false;
           if (j + 1 < n) {
             // dP(j+1) once dP(j) is in the element-wise warps' registers;
             // this commit also covers S(j+1), issued one key tile earlier.
@@ -862,6 +862,11 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             const bool have_v = mbar_try_wait(bar(L::B_FULL + s3), ph3);
             const bool have_dpr = mbar_try_wait(bar(L::B_DPR), s & 1);
             have_p = mbar_test_wait(bar(L::B_P), s & 1);
+            if (j + 2 < n) {
+              uint32_t s4l, ph4l;
+              at(4, s4l, ph4l);
+              look_k = mbar_test_wait(bar(L::B_FULL + s4l), ph4l);
+            }
             if ((!have_v && !mbar_wait_bounded(bar(L::B_FULL + s3), ph3, abort, lim)) ||
                 (!have_dpr && !mbar_wait_bounded(bar(L::B_DPR), s & 1, abort, lim))) {
               ok = false;
@@ -881,8 +886,9 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
           mma_dq(j, kv_at(bs));
           mma_commit(bar(L::B_EMPTY + bs));
           if (j + 2 < n) {
-            uint32_t s4;
-            if (!full_at(4, s4)) {
+            uint32_t s4, ph4;
+            at(4, s4, ph4);
+            if (!look_k && !mbar_wait_bounded(bar(L::B_FULL + s4), ph4, abort, lim)) {
               ok = false;
               break;
             }
