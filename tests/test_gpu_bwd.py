@@ -48,7 +48,9 @@ def _run(sl, sq, sk, H, Hk, d, seed, scale=None):
 
 @pytest.mark.parametrize("seed,sq,sk,H,Hk,d", [
     (0, 512, 512, 2, 1, 128), (1, 1000, 1100, 4, 2, 64), (2, 700, 1300, 2, 2, 128),
-    (3, 1300, 600, 3, 1, 64), (4, 1536, 1536, 2, 2, 128), (5, 129, 257, 1, 1, 128)])
+    (3, 1300, 600, 3, 1, 64), (4, 1536, 1536, 2, 2, 128), (5, 129, 257, 1, 1, 128),
+    # S_q = 640: the last query tile's second half starts exactly at S_q
+    (6, 640, 700, 2, 1, 128)])
 def test_fuzzed_slices_all_kinds(seed, sq, sk, H, Hk, d):
     sl = W.random_slices(sq, sk, 30, seed=seed + 100, unit=1, max_len=max(16, min(sq, sk) // 2))
     _run(sl, sq, sk, H, Hk, d, seed)
